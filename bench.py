@@ -1,0 +1,406 @@
+"""Benchmark of the blockwise-FP8 ZeRO-1 optimizer step on one GB300.
+
+One step = one pass of the whole hot path over the shard, through the C-ABI:
+fold the row-major FP32 grads into blocks -> global grad norm + inf flag ->
+fused unscale + clip + AdamW + per-block E4M3 quantise -> unfold the codes
+into the row-major FP8 weights -> host reads found_inf and updates the loss
+scale.  Workload (default): 32 experts x gate_up [7168,4096] + down [2048,7168]
+(86016 blocks, 1.41 G padded elements, ~31 GB resident), one DP rank owning the
+whole buffer.  Inputs are larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs the same
+single-GPU workload as an independent replica; the timing is the max over
+ranks and ``value`` counts the elements of all ranks.  ``--impl reference``
+times the CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp8z1_step elements/s and achieved HBM GB/s (fraction of ~8 TB/s) per shard, 1 GB300"
+# bytes the fused step must move per padded element: read grad, master, m, v
+# (16) + write master, m, v (12) + write the E4M3 code (1); plus 4 per block (scale)
+STEP_BYTES_PER_ELEM = 29
+STEP_BYTES_PER_BLOCK = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _ncu_traffic():
+    """Per-launch DRAM bytes of the step kernel from the committed ncu summary."""
+    p = os.path.join(ROOT, "profiles", "step_kernel_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def bench_ours(args, rank, world, dist):
+    import torch
+
+    from blockwise_fp8_zero_fold_gb300 import build as fp8build
+    from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
+    from blockwise_fp8_zero_fold_gb300 import synth
+    from blockwise_fp8_zero_fold_gb300.optimizer import ShardOptimizer
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fp8build.build()
+    if dist is not None:
+        dist.barrier()
+    F.lib()
+
+    w = synth.workload(args.workload, dp=1, rank=0)
+    if args.experts:
+        w = synth.workload(args.workload, dp=1, rank=0,
+                           shapes=[(min(e, args.experts), r, c) for e, r, c in w.shapes])
+    opt = ShardOptimizer(w.shapes, dp_size=1, rank=0, device=dev, loss_scale=w.loss_scale,
+                         growth_interval=w.growth_interval,
+                         **{k: v for k, v in w.hp().items() if k != "loss_scale"})
+    for kind, buf in (("master", None), ("m", None), ("v", None)):
+        rm = synth.make_state(w, kind, dev)
+        opt.fold_into(rm, {"master": opt.master, "m": opt.m, "v": opt.v}[kind])
+        del rm
+    grads = synth.make_grads(w, 1, dev)
+    fp8 = [torch.zeros(s, dtype=torch.uint8, device=dev) for s in w.shapes]
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    n_pad, n_real, nblk = opt.n_padded, opt.n_real, opt.nblk
+
+    # warm-up
+    for _ in range(args.warmup):
+        opt.step(grads, fp8)
+    torch.cuda.synchronize()
+
+    # timed region: K whole-path steps, per-kernel events on the launching stream
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for k in ("fold", "norm", "step", "unfold")}
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    skipped = 0
+    for i in range(args.steps):
+        e = ev["fold"][i]
+        e[0].record(stream)
+        opt.fold_into(grads, opt.grad)
+        e[1].record(stream)
+        opt.sumsq.zero_()
+        opt.found_inf.zero_()
+        e = ev["norm"][i]
+        e[0].record(stream)
+        F.fp8z1_grad_norm(opt.layout, opt.grad, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
+        e[1].record(stream)
+        hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
+        e = ev["step"][i]
+        e[0].record(stream)
+        F.fp8z1_step(opt.layout, hp, opt.grad, opt.master, opt.m, opt.v, opt.codes, opt.scales,
+                     opt.b0, opt.b1, opt.sumsq, opt.found_inf)
+        e[1].record(stream)
+        e = ev["unfold"][i]
+        e[0].record(stream)
+        opt.unfold_from(opt.codes, fp8)
+        e[1].record(stream)
+        skipped += opt.finish_step()  # host reads found_inf (a10)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    ms_per_step = elapsed_ms / args.steps
+    value = world * n_pad * args.steps / (elapsed_ms / 1e3)
+
+    peak, peak_kind = _peak_hbm()
+    step_bytes = STEP_BYTES_PER_ELEM * n_pad + STEP_BYTES_PER_BLOCK * nblk
+    achieved = step_bytes / (kern["step"] / 1e3) / 1e9
+    fold_bytes = 4 * (n_real + n_pad)
+    unfold_bytes = 1 * (n_real + n_pad)
+    norm_bytes = 4 * n_pad
+    tr = _ncu_traffic()
+    traffic = None
+    if tr and tr.get("workload") == args.workload and tr.get("source_sha") == _step_source_sha():
+        traffic = tr.get("bytes_per_launch")
+
+    # e2e: the same step through the public API, grads from pinned host memory
+    # and the FP8 weights + scales + found flag read back every step
+    e2e = None
+    if args.e2e_steps > 0:
+        hgrads = [torch.empty(s, dtype=torch.float32, pin_memory=True) for s in w.shapes]
+        for h, d in zip(hgrads, grads):
+            h.copy_(d)
+        hfp8 = [torch.empty(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
+        hscales = torch.empty(nblk, dtype=torch.float32, pin_memory=True)
+        hflag = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        h2d = sum(h.numel() * 4 for h in hgrads)
+        d2h = sum(h.numel() for h in hfp8) + nblk * 4 + 4
+
+        def e2e_step():
+            for d, h in zip(grads, hgrads):
+                d.copy_(h, non_blocking=True)
+            opt.launch_step(grads, fp8)
+            for h, d in zip(hfp8, fp8):
+                h.copy_(d, non_blocking=True)
+            hscales.copy_(opt.scales, non_blocking=True)
+            hflag.copy_(opt.found_inf, non_blocking=True)
+            torch.cuda.synchronize()
+            F.fp8z1_scaler_update(opt.scaler, int(hflag.item()))
+
+        e2e_step()
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        wall = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([wall], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            wall = float(t.item())
+        e2e = {"value": world * n_pad * args.e2e_steps / wall, "unit": "elem/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": wall / args.e2e_steps * 1e3, "steps": args.e2e_steps}
+        del hgrads, hfp8
+
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "elem/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
+        "config": {
+            "workload": f"{args.workload}{'' if not args.experts else f'[{args.experts} experts]'}: " + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
+            "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "dp": "whole buffer (1 rank)",
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (~31 GB resident per step), no flush",
+            "value_counts": "padded elements per second through the whole step",
+        },
+        "gpu_launches": 4 * args.steps,
+        "kernels_ms": kern,
+        "kernels_gbs": {"fold": fold_bytes / kern["fold"] / 1e6, "norm": norm_bytes / kern["norm"] / 1e6,
+                        "step": achieved, "unfold": unfold_bytes / kern["unfold"] / 1e6},
+        "step_kernel_elem_per_s": n_pad / (kern["step"] / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "fp8z1_step", "peak_source": peak_kind,
+                     "bytes_per_launch": step_bytes},
+        "clocks": clk,
+        "skipped_steps": skipped,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
+        out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)
+    return out
+
+
+def _step_source_sha():
+    import hashlib
+    p = os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", "step.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class OracleSample:
+    """The oracle (single thread) on the first ``experts`` experts of each MoE
+    param, over the whole path: fold grads, exact norm, step, unfold codes.
+    Inputs are drawn once; run() times one pass."""
+
+    def __init__(self, workload: str, experts: int):
+        import numpy as np
+
+        import oracle
+        from blockwise_fp8_zero_fold_gb300 import synth
+
+        w = synth.workload(workload)
+        self.shapes = [(min(e, experts), r, c) for e, r, c in w.shapes]
+        self.w = synth.workload(workload, shapes=self.shapes)
+        fold = oracle.fold
+        self.p = fold(self.shapes, [t.numpy() for t in synth.make_state(self.w, "master", "cpu")])
+        self.m = fold(self.shapes, [t.numpy() for t in synth.make_state(self.w, "m", "cpu")])
+        self.v = fold(self.shapes, [t.numpy() for t in synth.make_state(self.w, "v", "cpu")])
+        self.g_rows = [t.numpy() for t in synth.make_grads(self.w, 1, "cpu")]
+        self.outs = [np.zeros(s, np.uint8) for s in self.shapes]
+        self.n_pad = self.p.size
+        self.t = 0
+        self.sample = (f"{workload}, first {experts} expert(s) of each param ({self.n_pad} padded "
+                       f"elements); whole path: fold grads, exact norm, step, unfold codes")
+
+    def run(self) -> float:
+        import oracle
+
+        self.t += 1
+        t0 = time.perf_counter()
+        g = oracle.fold(self.shapes, self.g_rows)
+        s, f = oracle.sumsq(g)
+        q, _, _ = oracle.step(oracle.make_hp(step=self.t, **self.w.hp()), s, f, g, self.p, self.m, self.v)
+        oracle.unfold(self.shapes, q, self.outs)
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(workload: str, experts: int):
+    s = OracleSample(workload, experts)
+    t = s.run()
+    return {"value": s.n_pad / t, "unit": "elem/s", "cores": 1, "kind": "oracle",
+            "sample": s.sample, "seconds": t, "cpu": _cpu_name()}
+
+
+def _cpu_name():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return os.uname().machine
+
+
+def bench_reference(args, rank, world):
+    """The oracle as the reference arm, on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    smp = OracleSample(args.workload, args.ref_sample_experts)
+    for _ in range(args.warmup):
+        smp.run()
+    ts = [smp.run() for _ in range(args.steps)]
+    v = smp.n_pad * len(ts) / sum(ts)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": v, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sum(ts) / len(ts) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload} (oracle on a bounded sample: {smp.sample})"},
+        "cpu_baseline": {"value": v, "unit": "elem/s", "cores": 1, "kind": "oracle",
+                         "sample": smp.sample, "cpu": _cpu_name()},
+        "e2e": {"value": v, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="moe")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="keep only the first K experts of each 3-D param (a smaller case)")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-sample-experts", type=int, default=6)
+    ap.add_argument("--ref-sample-experts", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        out = bench_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        td.init_process_group("nccl")
+        dist = td
+    out = bench_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,51 @@
+// Internal definitions shared by the translation units of libfp8z1.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "fp8z1.h"
+
+// Device-side status bits, OR-ed into the layout's status word by a kernel
+// that meets device data it cannot use (it then skips that work).
+#define FP8Z1_DEV_BADPTR 1u  // a param pointer was null or not elem_size aligned
+
+struct fp8z1_layout {
+    std::vector<fp8z1_shape> shapes;
+    std::vector<fp8z1_block> lut;  // host copy of the block lookup table
+    int32_t n_params = 0;
+    int32_t dp_size = 1;
+    int64_t n_blocks = 0;
+    int64_t n_real = 0;
+    bool on_device = false;
+    int device = -1;
+    int sm_count = 0;
+    fp8z1_block* d_lut = nullptr;      // device copy of `lut`
+    double* d_partials = nullptr;      // grad-norm workspace: one double per CTA
+    unsigned* d_counter = nullptr;     // grad-norm workspace: CTAs finished
+    unsigned* d_status = nullptr;      // FP8Z1_DEV_* bits
+    int max_partials = 0;
+};
+
+namespace fp8z1 {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Common checks of a layout and a block range for the device entry points.
+inline int check_range(const fp8z1_layout* L, int64_t b0, int64_t b1)
+{
+    if (!L) return FP8Z1_EINVAL;
+    if (b0 < 0 || b1 < b0 || b1 > L->n_blocks) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    return FP8Z1_OK;
+}
+
+inline int launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FP8Z1_OK : FP8Z1_ECUDA;
+}
+
+}  // namespace fp8z1

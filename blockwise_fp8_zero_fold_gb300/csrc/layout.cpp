@@ -1,0 +1,200 @@
+// Host side of libfp8z1.so: the block lookup table, shard ranges, the loss
+// scaler and status text.
+//
+// "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §块粒度切分: each quantised dim
+// is padded up to a multiple of 128, a lookup table records every 128x128
+// block's param and real extent, and ZeRO shards are cut on block edges;
+// §参数布局变换: block order of fold is (expert, row block, col block).
+#include <limits.h>
+
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int64_t kTile = FP8Z1_TILE;
+
+int64_t tiles(int64_t n) { return (n + kTile - 1) / kTile; }
+
+// Free whatever device memory a layout holds (safe on partial layouts).
+void release_device(fp8z1_layout* L)
+{
+    cudaFree(L->d_lut);
+    cudaFree(L->d_partials);
+    cudaFree(L->d_counter);
+    cudaFree(L->d_status);
+    L->d_lut = nullptr;
+    L->d_partials = nullptr;
+    L->d_counter = nullptr;
+    L->d_status = nullptr;
+}
+
+int upload(fp8z1_layout* L)
+{
+    if (cudaGetDevice(&L->device) != cudaSuccess) return FP8Z1_ECUDA;
+    if (cudaDeviceGetAttribute(&L->sm_count, cudaDevAttrMultiProcessorCount, L->device) != cudaSuccess)
+        return FP8Z1_ECUDA;
+    // grad-norm workspace: up to 4 CTAs per SM, capped at 4096 partial sums
+    L->max_partials = L->sm_count * 4 < 4096 ? L->sm_count * 4 : 4096;
+    const size_t lut_bytes = sizeof(fp8z1_block) * (size_t)L->n_blocks;
+    if (cudaMalloc(&L->d_lut, lut_bytes ? lut_bytes : sizeof(fp8z1_block)) != cudaSuccess ||
+        cudaMalloc(&L->d_partials, sizeof(double) * (size_t)L->max_partials) != cudaSuccess ||
+        cudaMalloc(&L->d_counter, sizeof(unsigned)) != cudaSuccess ||
+        cudaMalloc(&L->d_status, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ENOMEM;
+    }
+    if (lut_bytes && cudaMemcpy(L->d_lut, L->lut.data(), lut_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
+        return FP8Z1_ECUDA;
+    if (cudaMemset(L->d_counter, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(L->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return FP8Z1_ECUDA;
+    L->on_device = true;
+    return FP8Z1_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                                  uint32_t flags, fp8z1_layout** out)
+{
+    if (!out) return FP8Z1_EINVAL;
+    *out = nullptr;
+    if (!shapes || n_params < 1 || dp_size < 1 || (flags & ~FP8Z1_LAYOUT_HOST_ONLY)) return FP8Z1_EINVAL;
+    // validate shapes and count blocks without overflowing int64
+    int64_t nblk = 0, nreal = 0;
+    const int64_t kMax = INT64_MAX / FP8Z1_BLOCK_ELEMS;
+    for (int32_t i = 0; i < n_params; ++i) {
+        const fp8z1_shape s = shapes[i];
+        if (s.E < 1 || s.R < 1 || s.C < 1 || s.C > INT_MAX || s.E > INT_MAX || tiles(s.R) > INT_MAX)
+            return FP8Z1_EINVAL;
+        const int64_t rb = tiles(s.R), cb = tiles(s.C);
+        if (rb > kMax / cb || s.E > kMax / (rb * cb)) return FP8Z1_EINVAL;
+        const int64_t nb = s.E * rb * cb;
+        if (nb > kMax - nblk) return FP8Z1_EINVAL;
+        nblk += nb;
+        nreal += s.E * s.R * s.C;  // <= padded count, which fits
+    }
+    fp8z1_layout* L = new (std::nothrow) fp8z1_layout();
+    if (!L) return FP8Z1_ENOMEM;
+    try {
+        L->shapes.assign(shapes, shapes + n_params);
+        L->lut.resize((size_t)nblk);
+    } catch (...) {
+        delete L;
+        return FP8Z1_ENOMEM;
+    }
+    L->n_params = n_params;
+    L->dp_size = dp_size;
+    L->n_blocks = nblk;
+    L->n_real = nreal;
+    int64_t k = 0;
+    for (int32_t i = 0; i < n_params; ++i) {
+        const fp8z1_shape s = shapes[i];
+        const int64_t rbs = tiles(s.R), cbs = tiles(s.C);
+        for (int64_t e = 0; e < s.E; ++e)
+            for (int64_t rb = 0; rb < rbs; ++rb)
+                for (int64_t cb = 0; cb < cbs; ++cb) {
+                    fp8z1_block& b = L->lut[(size_t)k++];
+                    b.src_offset = (e * s.R + kTile * rb) * s.C + kTile * cb;
+                    b.param = i;
+                    b.expert = (int32_t)e;
+                    b.row_block = (int32_t)rb;
+                    b.col_block = (int32_t)cb;
+                    b.ld = (int32_t)s.C;
+                    const int64_t rr = s.R - kTile * rb, cr = s.C - kTile * cb;
+                    b.rows_real = (int16_t)(rr < kTile ? rr : kTile);
+                    b.cols_real = (int16_t)(cr < kTile ? cr : kTile);
+                }
+    }
+    if (!(flags & FP8Z1_LAYOUT_HOST_ONLY)) {
+        const int st = upload(L);
+        if (st != FP8Z1_OK) {
+            release_device(L);
+            delete L;
+            return st;
+        }
+    }
+    *out = L;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_destroy_layout(fp8z1_layout* L)
+{
+    if (!L) return FP8Z1_OK;
+    if (L->on_device) release_device(L);
+    delete L;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_layout_info(const fp8z1_layout* L, int64_t* n_blocks, int64_t* n_elems_padded,
+                                 int64_t* n_elems_real)
+{
+    if (!L) return FP8Z1_EINVAL;
+    if (n_blocks) *n_blocks = L->n_blocks;
+    if (n_elems_padded) *n_elems_padded = L->n_blocks * FP8Z1_BLOCK_ELEMS;
+    if (n_elems_real) *n_elems_real = L->n_real;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_shard_range(const fp8z1_layout* L, int32_t rank, int64_t* b0, int64_t* b1)
+{
+    if (!L || !b0 || !b1 || rank < 0 || rank >= L->dp_size) return FP8Z1_EINVAL;
+    const int64_t per = (L->n_blocks + L->dp_size - 1) / L->dp_size;
+    int64_t lo = per * rank, hi = per * (rank + 1);
+    *b0 = lo < L->n_blocks ? lo : L->n_blocks;
+    *b1 = hi < L->n_blocks ? hi : L->n_blocks;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_copy_lut(const fp8z1_layout* L, fp8z1_block* host_dst, int64_t capacity)
+{
+    if (!L || (!host_dst && L->n_blocks) || capacity < L->n_blocks) return FP8Z1_EINVAL;
+    for (int64_t k = 0; k < L->n_blocks; ++k) host_dst[k] = L->lut[(size_t)k];
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_device_status(const fp8z1_layout* L, uint32_t* bits)
+{
+    if (!L || !bits) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, L->d_status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(L->d_status, 0, sizeof v) != cudaSuccess)
+        return FP8Z1_ECUDA;
+    *bits = v;
+    return FP8Z1_OK;
+}
+
+// "DeepSpeed ZeRO 优化" §六 Loss Scaling: an overflow halves S and skips the
+// step; N clean steps in a row double S.
+extern "C" int fp8z1_scaler_update(fp8z1_loss_scaler* s, int32_t found_inf)
+{
+    if (!s || !(s->scale > 0.0f) || s->growth_interval < 1) return FP8Z1_EINVAL;
+    if (found_inf) {
+        s->scale *= 0.5f;
+        s->good_steps = 0;
+        return FP8Z1_OK;
+    }
+    s->step += 1;
+    if (++s->good_steps >= s->growth_interval) {
+        s->scale *= 2.0f;
+        s->good_steps = 0;
+    }
+    return FP8Z1_OK;
+}
+
+extern "C" const char* fp8z1_strerror(int status)
+{
+    switch (status) {
+    case FP8Z1_OK: return "ok";
+    case FP8Z1_EINVAL: return "invalid argument";
+    case FP8Z1_EALIGN: return "misaligned pointer";
+    case FP8Z1_ENOMEM: return "out of memory";
+    case FP8Z1_ECUDA: return "CUDA runtime error";
+    case FP8Z1_ENODEV: return "layout has no device tables (built host-only)";
+    default: return "unknown status";
+    }
+}

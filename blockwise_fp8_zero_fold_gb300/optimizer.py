@@ -1,0 +1,114 @@
+"""One DP rank's blockwise-FP8 ZeRO-1 optimizer, sequencing the C-ABI calls.
+
+"面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结 gives the order this class
+follows on its shard [b0, b1):
+  init : fold the row-major FP32 master params (and moments) into the 1-D
+         block buffers of the shard (§参数布局变换, §块粒度切分);
+  step : fold the (reduced) row-major grads of the shard, global grad norm
+         ("DeepSpeed ZeRO 优化" §七), fused unscale + clip + AdamW + per-block
+         E4M3 quantise, unfold the codes back into the row-major FP8 params;
+         the scales need no unfold: block order (e, rb, cb) makes the scale
+         buffer of a param a [E, R/128, C/128] view.
+  host : read found_inf and update the loss scale / step count (§六).
+Every step of the path runs in libfp8z1.so; this class only owns torch
+buffers and calls the entry points in order.  One process, one GPU: with
+dp_size > 1 the other ranks' norm partials come through ``norm_hook``.
+"""
+from __future__ import annotations
+
+from typing import Callable, List, Optional, Sequence
+
+import torch
+
+from . import fp8z1 as F
+
+
+class ShardOptimizer:
+    def __init__(self, shapes: Sequence[Sequence[int]], *, dp_size: int = 1, rank: int = 0,
+                 lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=1.0,
+                 loss_scale=1024.0, growth_interval=1000, device="cuda"):
+        self.device = torch.device(device)
+        self.layout = F.fp8z1_build_layout(shapes, dp_size)
+        self.shapes = self.layout.shapes
+        self.b0, self.b1 = F.fp8z1_shard_range(self.layout, rank)
+        self.nblk, self.n_padded, self.n_real = F.fp8z1_layout_info(self.layout)
+        nb = self.b1 - self.b0
+        n = nb * F.BLOCK_ELEMS
+        kw = dict(device=self.device)
+        self.master = torch.zeros(n, dtype=torch.float32, **kw)
+        self.m = torch.zeros(n, dtype=torch.float32, **kw)
+        self.v = torch.zeros(n, dtype=torch.float32, **kw)
+        self.grad = torch.zeros(n, dtype=torch.float32, **kw)
+        self.codes = torch.zeros(n, dtype=torch.uint8, **kw)
+        self.scales = torch.ones(nb, dtype=torch.float32, **kw)
+        self.sumsq = torch.zeros(1, dtype=torch.float64, **kw)
+        self.found_inf = torch.zeros(1, dtype=torch.int32, **kw)
+        self.hp = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
+                       max_norm=max_norm)
+        self.scaler = F.fp8z1_loss_scaler(float(loss_scale), 0, 0, int(growth_interval))
+        self.norm_hook: Optional[Callable[[torch.Tensor, torch.Tensor], None]] = None
+        self._ptr_cache = {}
+
+    # -- pointer arrays for fold/unfold ------------------------------------
+    def _ptrs(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
+        assert len(tensors) == len(self.shapes)
+        key = tuple(t.data_ptr() for t in tensors)
+        hit = self._ptr_cache.get(key)
+        if hit is None:
+            hit = F.param_pointers(tensors, self.device)
+            self._ptr_cache[key] = hit
+        return hit
+
+    def fold_into(self, params: Sequence[torch.Tensor], dst: torch.Tensor, stream=None):
+        esz = params[0].element_size()
+        F.fp8z1_fold(self.layout, self._ptrs(params), dst, esz, self.b0, self.b1, stream)
+
+    def unfold_from(self, src: torch.Tensor, params: Sequence[torch.Tensor], stream=None):
+        esz = params[0].element_size()
+        F.fp8z1_unfold(self.layout, src, self._ptrs(params), esz, self.b0, self.b1, stream)
+
+    # -- state --------------------------------------------------------------
+    def init_state(self, master: Sequence[torch.Tensor], m=None, v=None, stream=None):
+        """Fold row-major FP32 params (and optionally moments) into the shard."""
+        self.fold_into(master, self.master, stream)
+        if m is not None:
+            self.fold_into(m, self.m, stream)
+        if v is not None:
+            self.fold_into(v, self.v, stream)
+
+    def scale_views(self) -> List[torch.Tensor]:
+        """Per-param [E, ceil(R/128), ceil(C/128)] views of the scale buffer
+        (whole-buffer shards only)."""
+        assert self.b0 == 0 and self.b1 == self.nblk
+        out, off = [], 0
+        for e, r, c in self.shapes:
+            rb, cb = -(-r // 128), -(-c // 128)
+            out.append(self.scales[off:off + e * rb * cb].view(e, rb, cb))
+            off += e * rb * cb
+        return out
+
+    # -- one step -------------------------------------------------------------
+    def launch_step(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
+                    stream=None):
+        """Enqueue one step (no host synchronisation)."""
+        self.fold_into(grads, self.grad, stream)
+        self.sumsq.zero_()
+        self.found_inf.zero_()
+        F.fp8z1_grad_norm(self.layout, self.grad, self.b0, self.b1, self.sumsq, self.found_inf, stream)
+        if self.norm_hook is not None:
+            self.norm_hook(self.sumsq, self.found_inf)
+        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
+        F.fp8z1_step(self.layout, hp, self.grad, self.master, self.m, self.v, self.codes, self.scales,
+                     self.b0, self.b1, self.sumsq, self.found_inf, stream)
+        if fp8_params is not None:
+            self.unfold_from(self.codes, fp8_params, stream)
+
+    def finish_step(self) -> int:
+        """Read found_inf (synchronises) and update the loss scale and t."""
+        found = int(self.found_inf.item())
+        F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
+    def step(self, grads, fp8_params=None, stream=None) -> int:
+        self.launch_step(grads, fp8_params, stream)
+        return self.finish_step()

@@ -1,0 +1,212 @@
+/*
+ * fp8z1.h -- C ABI of libfp8z1.so: the ZeRO-1 optimizer step for
+ * blockwise-FP8 weights, on one data-parallel rank's shard, on one GB300
+ * (sm_103a).
+ *
+ * Method: "面向 Blockwise FP8 量化的 ZeRO 优化器设计" (A ZeRO Optimizer Design
+ * for Blockwise FP8 Quantization):
+ *   §Blockwise 量化         one FP32 scale per 128x128 block of a weight;
+ *   §块粒度切分             pad each quantised dim to a multiple of 128, keep a
+ *                           block lookup table, shard on block edges;
+ *   §参数布局变换           fold / unfold between row-major [E,R,C] and a
+ *                           128x128-block-contiguous 1-D buffer;
+ *   §总结                   fold grads -> slice -> elementwise update ->
+ *                           quantise FP8 + scales from the FP32 master -> unfold.
+ * Step order, clipping and loss scaling: "DeepSpeed ZeRO 优化" §三 (global
+ * norm -> loss-scale update -> unscale+clip -> update -> low-precision copy),
+ * §六 Loss Scaling, §七 梯度裁剪.
+ *
+ * Conventions (all entry points):
+ *   - A block is 128 x 128 = 16384 elements (FP8Z1_BLOCK_ELEMS).  Blocks are
+ *     numbered over the params in the order given to fp8z1_build_layout, and
+ *     inside a param [E,R,C] in (e, row block, col block) row-major order.
+ *   - A shard is a block range [b0, b1).  Every *_shard pointer points at
+ *     block b0 of its buffer and holds (b1 - b0) * 16384 elements
+ *     (scale_shard: b1 - b0 floats).  Shard pointers must be 16-byte aligned.
+ *   - The caller owns every device buffer it passes; the library owns only the
+ *     layout (host tables, the device lookup table, a small norm workspace).
+ *   - Calls that take a `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) only enqueue work on it and never synchronise.  Asynchronous
+ *     device faults surface at the caller's next synchronisation, as in CUDA.
+ *   - Every call returns FP8Z1_OK (0) or a negative status; arguments are
+ *     checked on the host before anything is enqueued, and a rejected call
+ *     enqueues nothing.  No exception crosses the ABI; nothing aborts.
+ *   - Floating point: IEEE FP32 for the update (explicit fused multiply-adds,
+ *     correctly rounded division and square root), double for the norm scalars.
+ */
+#ifndef FP8Z1_H
+#define FP8Z1_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8Z1_TILE 128
+#define FP8Z1_BLOCK_ELEMS 16384
+
+/* status codes */
+#define FP8Z1_OK 0
+#define FP8Z1_EINVAL (-1) /* bad argument: null, bad range/shape/elem_size, hp out of domain */
+#define FP8Z1_EALIGN (-2) /* a pointer is not aligned as required */
+#define FP8Z1_ENOMEM (-3) /* host or device allocation failed */
+#define FP8Z1_ECUDA (-4)  /* a CUDA runtime call or kernel launch failed */
+#define FP8Z1_ENODEV (-5) /* the layout was built host-only and has no device tables */
+
+/* fp8z1_build_layout flags */
+#define FP8Z1_LAYOUT_HOST_ONLY 1u /* build the tables on the host only (no CUDA call) */
+
+typedef struct fp8z1_layout fp8z1_layout; /* opaque, owned by the library */
+
+/* Shape of one quantised param: row-major [E, R, C]; a 2-D weight has E = 1.
+ * E, R, C >= 1 and C < 2^31. */
+typedef struct {
+    int64_t E, R, C;
+} fp8z1_shape;
+
+/* One entry of the block lookup table (32 bytes):
+ * §块粒度切分 -- the table that maps a flat block index to its param and its
+ * real (unpadded) extent, so the 1-D buffers can be walked param by param. */
+typedef struct {
+    int64_t src_offset; /* element offset of the block's (0,0) element in its
+                           param's row-major storage: (e*R + 128*rb)*C + 128*cb */
+    int32_t param;      /* index into the shape list */
+    int32_t expert;     /* e */
+    int32_t row_block;  /* rb */
+    int32_t col_block;  /* cb */
+    int32_t ld;         /* row stride of the param in elements (= C) */
+    int16_t rows_real;  /* min(128, R - 128*rb) */
+    int16_t cols_real;  /* min(128, C - 128*cb) */
+} fp8z1_block;
+
+/* AdamW + clipping + loss-scale hyper-parameters of one step (read on the
+ * host at call time).  The pages fix none of the AdamW details; the reading
+ * is decoupled weight decay with bias correction:
+ *   g = g_s / loss_scale, then g *= clip_coef when clip_coef < 1,
+ *   clip_coef = max_norm / (||g_s|| / loss_scale + 1e-6)        (§七)
+ *   m = beta1 m + (1-beta1) g;   v = beta2 v + (1-beta2) g^2
+ *   p = p (1 - lr wd) - lr * (m / (1-beta1^t)) / (sqrt(v / (1-beta2^t)) + eps)
+ * Domain: lr >= 0, 0 <= beta1, beta2 < 1, eps > 0, weight_decay >= 0,
+ * max_norm > 0 (+inf disables clipping), loss_scale > 0 and finite (a power of
+ * two makes g_s * (clip / loss_scale) bit-identical to unscale-then-clip),
+ * step = t >= 1 (the 1-based index of the step being taken). */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, max_norm, loss_scale;
+    int64_t step;
+} fp8z1_adamw_hp;
+
+/* Dynamic loss scaling state, updated on the host after each step (§六). */
+typedef struct {
+    float scale;             /* S, > 0 */
+    int64_t step;            /* completed (not skipped) steps t */
+    int32_t good_steps;      /* clean steps since S last changed */
+    int32_t growth_interval; /* N >= 1: S doubles after N clean steps in a row */
+} fp8z1_loss_scaler;
+
+/* ---- layout (§块粒度切分, §参数布局变换) ------------------------------------ */
+
+/* Build the block LUT and the shard ranges of `n_params` params for DP size
+ * `dp_size`, and (unless FP8Z1_LAYOUT_HOST_ONLY) upload the LUT to the current
+ * CUDA device with synchronous copies.  Shard of rank r: S = ceil(nblk / D)
+ * blocks, [r*S, min((r+1)*S, nblk)) (the last ranks may be short or empty).
+ * `shapes`: host array of n_params >= 1 shapes; dp_size >= 1.
+ * On success *out receives a layout that fp8z1_destroy_layout frees.
+ * Errors: EINVAL (null, n_params < 1, dp_size < 1, a dim < 1, C >= 2^31, an
+ * element count that overflows int64), ENOMEM, ECUDA. */
+int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                       uint32_t flags, fp8z1_layout** out);
+
+/* Free a layout and its device tables (NULL is accepted).  Call only when no
+ * work that uses it is still running on the device. */
+int fp8z1_destroy_layout(fp8z1_layout* layout);
+
+/* Totals: blocks, padded elements (= blocks * 16384) and real elements. */
+int fp8z1_layout_info(const fp8z1_layout* layout, int64_t* n_blocks, int64_t* n_elems_padded,
+                      int64_t* n_elems_real);
+
+/* Block range [*b0, *b1) of DP rank `rank` (0 <= rank < dp_size). */
+int fp8z1_shard_range(const fp8z1_layout* layout, int32_t rank, int64_t* b0, int64_t* b1);
+
+/* Copy the LUT (n_blocks entries) to host memory; `capacity` is the number
+ * of entries `host_dst` holds (EINVAL when too small). */
+int fp8z1_copy_lut(const fp8z1_layout* layout, fp8z1_block* host_dst, int64_t capacity);
+
+/* Read and clear the layout's device status word (synchronous; waits for the
+ * copy).  Bit 1 (FP8Z1_DEVSTATUS_BADPTR): a fold/unfold met a param pointer
+ * in its device pointer array that was null or not elem_size aligned, and
+ * skipped the blocks of that param.  0 means no such event since the last read.
+ * Errors: EINVAL, ENODEV, ECUDA. */
+#define FP8Z1_DEVSTATUS_BADPTR 1u
+int fp8z1_device_status(const fp8z1_layout* layout, uint32_t* bits);
+
+/* ---- fold / unfold (§参数布局变换) ----------------------------------------- */
+
+/* fold: for every block k in [b0, b1) and (r, c) in 128 x 128,
+ *   dst_shard[(k - b0)*16384 + r*128 + c] = param[e][128*rb + r][128*cb + c]
+ * when the element is real, else 0 (the padding of §块粒度切分).
+ * `d_src_params`: DEVICE array of n_params DEVICE pointers, each to a
+ * row-major [E,R,C] param of `elem_size` bytes per element (1, 2 or 4), aligned
+ * to elem_size.  The copy is bitwise.  `dst_shard`: device, 16-byte aligned.
+ * An empty range (b0 == b1) enqueues nothing.
+ * Errors: EINVAL (null, elem_size, b0 > b1, b1 > n_blocks), EALIGN, ENODEV, ECUDA. */
+int fp8z1_fold(const fp8z1_layout* layout, const void* const* d_src_params, void* dst_shard,
+               int32_t elem_size, int64_t b0, int64_t b1, void* stream);
+
+/* unfold: the inverse of fold over the real elements of blocks [b0, b1):
+ * param[e][128*rb + r][128*cb + c] = src_shard[(k - b0)*16384 + r*128 + c].
+ * Padding is dropped; no element outside those blocks is written.
+ * `d_dst_params`: DEVICE array of n_params DEVICE pointers. */
+int fp8z1_unfold(const fp8z1_layout* layout, const void* src_shard, void* const* d_dst_params,
+                 int32_t elem_size, int64_t b0, int64_t b1, void* stream);
+
+/* ---- global grad norm ("DeepSpeed ZeRO 优化" §七, §六) --------------------- */
+
+/* Add the sum of squares of the FP32 loss-scaled grads of blocks [b0, b1) to
+ * *d_sumsq (device double; the caller zeroes it once per step and may then
+ * call this for several ranges, which stands in for the all-reduce of the
+ * per-rank partial sums), and OR 1 into *d_found_inf (device int32) when any
+ * of those grads is inf or nan.  Squares are formed exactly and summed in
+ * compensated single precision, then in double: the result is within about
+ * 1e-13 relative of the exact sum.  With found_inf set the sum is not
+ * meaningful.  Deterministic for a given device and range.
+ * The reduction uses a workspace owned by the layout: calls that share a
+ * layout must not overlap on the device (issue them on one stream).
+ * Errors: EINVAL, EALIGN, ENODEV, ECUDA. */
+int fp8z1_grad_norm(const fp8z1_layout* layout, const float* grad_shard, int64_t b0, int64_t b1,
+                    double* d_sumsq, int32_t* d_found_inf, void* stream);
+
+/* ---- fused step (§总结; "DeepSpeed ZeRO 优化" §三, §七) -------------------- */
+
+/* One optimizer step over blocks [b0, b1) of the shard, in one HBM pass:
+ * reads *d_sumsq (global) to form clip_coef on the device, unscales and clips
+ * the grads, applies AdamW to master/m/v in place, and for every block writes
+ * scale = amax|p_new| / 448 (1.0 when amax == 0) to scale_shard[k - b0] and
+ * the E4M3 codes of p_new / scale (round to nearest even, finite overflow
+ * saturates to +-448, sign kept) to fp8_shard.  When *d_found_inf != 0 the
+ * kernel writes nothing (the skipped step of §六): every buffer stays
+ * bit-identical.  `grad_shard` is not modified.
+ * Pointers: device; grad/master/m/v/fp8 16-byte aligned, scale 4-byte aligned.
+ * Errors: EINVAL (null, range, hp out of domain), EALIGN, ENODEV, ECUDA. */
+int fp8z1_step(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float* grad_shard,
+               float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+               float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
+               const int32_t* d_found_inf, void* stream);
+
+/* ---- loss scaling (host; "DeepSpeed ZeRO 优化" §六, §九 Q6) ---------------- */
+
+/* After a step whose found_inf flag the host has read: found_inf != 0 halves
+ * S, resets good_steps and leaves t unchanged (the step was skipped);
+ * otherwise t += 1 and, after growth_interval clean steps in a row, S doubles.
+ * Host only.  Errors: EINVAL (null, scale <= 0, growth_interval < 1). */
+int fp8z1_scaler_update(fp8z1_loss_scaler* scaler, int32_t found_inf);
+
+/* Static text for a status code. */
+const char* fp8z1_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Z1_H */

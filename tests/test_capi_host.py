@@ -1,0 +1,142 @@
+"""C-ABI host side, no GPU: the library loads, exports every declared symbol,
+and its host logic (block LUT, shard ranges, argument checks, loss scaler)
+agrees with the oracle."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from blockwise_fp8_zero_fold_gb300 import build as fp8build
+from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
+from blockwise_fp8_zero_fold_gb300 import synth
+from tests._golden import parse_shapes, rows
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    fp8build.build()  # nvcc cross-compiles without a GPU
+    return F.lib()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            text = open(os.path.join(inc, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fp8z1_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    names = _declared()
+    assert {"fp8z1_build_layout", "fp8z1_fold", "fp8z1_unfold", "fp8z1_grad_norm",
+            "fp8z1_step"} <= names
+    lib = C.CDLL(F.lib_path())
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+    assert names <= set(F._SIGS), "binding misses a declared entry point"
+
+
+LUT_CASES = [
+    [(1, 300, 200)],
+    [(3, 129, 257), (1, 1, 1), (2, 128, 128), (1, 17, 690)],
+    synth.workload("moe").shapes,
+    synth.ragged_shapes(200, seed=3),
+]
+
+
+@pytest.mark.parametrize("shapes", LUT_CASES, ids=lambda s: str(len(s)))
+def test_host_lut_bit_exact_against_oracle(shapes):
+    L = F.fp8z1_build_layout(shapes, dp_size=3, host_only=True)
+    nblk, padded, real = F.fp8z1_layout_info(L)
+    assert nblk == oracle.count_blocks(shapes) and padded == nblk * 16384
+    assert real == sum(e * r * c for e, r, c in shapes)
+    lut = F.fp8z1_copy_lut(L)
+    ref = oracle.build_lut(shapes)
+    assert np.array_equal(lut["param"], ref[:, 0])
+    assert np.array_equal(lut["expert"], ref[:, 1])
+    assert np.array_equal(lut["row_block"], ref[:, 2])
+    assert np.array_equal(lut["col_block"], ref[:, 3])
+    assert np.array_equal(lut["rows_real"], ref[:, 4])
+    assert np.array_equal(lut["cols_real"], ref[:, 5])
+    sh = np.array(shapes, dtype=np.int64)
+    R, Cc = sh[ref[:, 0], 1], sh[ref[:, 0], 2]
+    # element offset of the block's (0,0) element in its row-major param
+    assert np.array_equal(lut["src_offset"], (ref[:, 1] * R + 128 * ref[:, 2]) * Cc + 128 * ref[:, 3])
+    assert np.array_equal(lut["ld"], Cc)
+    for r in range(3):
+        assert F.fp8z1_shard_range(L, r) == oracle.shard_range(nblk, 3, r)
+
+
+@pytest.mark.parametrize("row", rows("layout_counts.txt"), ids=lambda r: f"{r[0]}-r{r[4]}")
+def test_golden_counts_and_ranges_through_abi(row):
+    name, shapes, nblk, dp, rank, b0, b1 = row
+    L = F.fp8z1_build_layout(parse_shapes(shapes), dp_size=int(dp), host_only=True)
+    assert F.fp8z1_layout_info(L)[0] == int(nblk)
+    assert F.fp8z1_shard_range(L, int(rank)) == (int(b0), int(b1))
+
+
+def test_argument_errors_enqueue_nothing():
+    lib = F.lib()
+    out = C.c_void_p()
+    bad = [[(0, 5, 5)], [(1, -1, 5)], [(1, 5, 1 << 31)]]
+    for shapes in bad:
+        arr = (F.fp8z1_shape * 1)(F.fp8z1_shape(*shapes[0]))
+        assert lib.fp8z1_build_layout(arr, 1, 1, 1, C.byref(out)) == F.EINVAL
+        assert out.value is None
+    arr = (F.fp8z1_shape * 1)(F.fp8z1_shape(1, 5, 5))
+    assert lib.fp8z1_build_layout(arr, 0, 1, 1, C.byref(out)) == F.EINVAL
+    assert lib.fp8z1_build_layout(arr, 1, 0, 1, C.byref(out)) == F.EINVAL
+    assert lib.fp8z1_build_layout(None, 1, 1, 1, C.byref(out)) == F.EINVAL
+    assert lib.fp8z1_build_layout(arr, 1, 1, 0x10, C.byref(out)) == F.EINVAL
+    L = F.fp8z1_build_layout([(1, 300, 200)], dp_size=2, host_only=True)
+    a, b = C.c_int64(), C.c_int64()
+    assert lib.fp8z1_shard_range(L.handle, 2, C.byref(a), C.byref(b)) == F.EINVAL
+    assert lib.fp8z1_shard_range(L.handle, -1, C.byref(a), C.byref(b)) == F.EINVAL
+    small = np.zeros(2, dtype=F.BLOCK_DTYPE)
+    assert lib.fp8z1_copy_lut(L.handle, small.ctypes.data, 2) == F.EINVAL
+    # device entry points on a host-only layout: checked and refused before any CUDA call
+    buf = np.zeros(64, np.uint8)
+    p = buf.ctypes.data
+    assert lib.fp8z1_fold(L.handle, p, p, 4, 0, 3, None) == F.ENODEV
+    assert lib.fp8z1_fold(L.handle, p, p, 3, 0, 3, None) == F.EINVAL
+    assert lib.fp8z1_fold(L.handle, p, p, 4, 2, 1, None) == F.EINVAL
+    assert lib.fp8z1_fold(L.handle, p, p, 4, 0, 7, None) == F.EINVAL
+    assert lib.fp8z1_unfold(L.handle, p, None, 4, 0, 3, None) == F.EINVAL
+    assert lib.fp8z1_grad_norm(L.handle, p, 0, 3, p, p, None) == F.ENODEV
+    hp = F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1024.0, 1)
+    assert lib.fp8z1_step(L.handle, C.byref(hp), p, p, p, p, p, p, 0, 3, p, p, None) == F.ENODEV
+    for badhp in [F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1024.0, 0),
+                  F.make_hp(1e-3, 1.0, 0.95, 1e-8, 0.1, 1.0, 1024.0, 1),
+                  F.make_hp(1e-3, 0.9, 0.95, 0.0, 0.1, 1.0, 1024.0, 1),
+                  F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 0.0, 1),
+                  F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 0.0, 1024.0, 1)]:
+        assert lib.fp8z1_step(L.handle, C.byref(badhp), p, p, p, p, p, p, 0, 3, p, p, None) == F.EINVAL
+    assert lib.fp8z1_device_status(L.handle, C.byref(C.c_uint32())) == F.ENODEV
+    assert F.fp8z1_strerror(F.EALIGN) == "misaligned pointer"
+    with pytest.raises(F.Fp8z1Error):
+        F.fp8z1_shard_range(L, 5)
+
+
+@pytest.mark.parametrize("row", rows("loss_scale_sequence.txt"))
+def test_scaler_matches_oracle_and_golden(row):
+    n, s0, flags, scales, steps = row
+    s = F.fp8z1_loss_scaler(float(s0), 0, 0, int(n))
+    ref = oracle.Scaler(float(s0), int(n))
+    got = []
+    for f in flags.split(","):
+        F.fp8z1_scaler_update(s, int(f))
+        ref.update(int(f))
+        assert (s.scale, s.step, s.good_steps) == (ref.scale, ref.step, ref.good_steps)
+        got.append((s.scale, s.step))
+    assert [g[0] for g in got] == [float(x) for x in scales.split(",")]
+    assert [g[1] for g in got] == [int(x) for x in steps.split(",")]
+    with pytest.raises(F.Fp8z1Error):
+        F.fp8z1_scaler_update(F.fp8z1_loss_scaler(0.0, 0, 0, 1), 0)
