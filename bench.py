@@ -155,6 +155,7 @@ def bench_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     t_start.record(stream)
     skipped = 0
     for i in range(args.steps):
@@ -180,6 +181,7 @@ def bench_ours(args, rank, world, dist):
         e[1].record(stream)
         skipped += opt.finish_step()  # host reads found_inf (a10)
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()

@@ -143,7 +143,7 @@ def test_subrange_writes_only_its_blocks_and_matches_split_ranks(lib):
     whole-buffer step bit for bit."""
     rng = np.random.default_rng(10)
     nb = 8
-    L = F.fp8z1_build_layout([(2, 512, 256)], dp_size=3)
+    L = F.fp8z1_build_layout([(2, 512, 128)], dp_size=3)
     assert F.fp8z1_layout_info(L)[0] == nb
     whole = Shard(nb, rng, m_sigma=1e-4, v_sigma=1e-8)
     split = Shard(nb, np.random.default_rng(10), m_sigma=1e-4, v_sigma=1e-8)
