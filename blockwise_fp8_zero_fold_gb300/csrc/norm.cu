@@ -22,6 +22,8 @@
 // deterministic for a given device and range.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace {
@@ -165,5 +167,81 @@ extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, i
     if (grid > L->max_partials) grid = L->max_partials;
     grad_norm_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4*>(grad_shard), n, L->d_partials, L->d_counter, d_sumsq, d_found_inf);
+    return fp8z1::launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// The same reduction for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: a framework whose caching
+// allocator already owns the device memory (a foreign cudaMalloc can fail, or
+// make the driver synchronise the device), or a step loop that must never
+// block on an allocation.  fp8z1_grad_norm takes its workspace from a layout,
+// which fp8z1_build_layout allocates.  This variant takes it from a file-scope
+// array instead, so it needs neither a layout nor any allocation.
+//
+// Workspace: one double per CTA plus the finished-CTA counter, in a static
+// array that every device which loads the library holds until the process
+// exits (8 * (4096 + 1) bytes).  Each CTA covers up to 64 blocks, so one call
+// covers at most 4096 * 64 = 262144 blocks; larger ranges are rejected (split
+// them into several calls, which accumulate into the same *d_sumsq).
+namespace {
+
+constexpr int64_t kNoAllocBlocksPerCta = 64;
+constexpr int kNoAllocMaxCtas = (int)(FP8Z1_NOALLOC_MAX_BLOCKS / kNoAllocBlocksPerCta);
+constexpr int kMaxDevices = 64;
+
+// partials[0, kNoAllocMaxCtas), then the counter (as an unsigned) in the last slot
+static __device__ __align__(256) double g_noalloc_scratch[kNoAllocMaxCtas + 1];
+
+std::mutex g_noalloc_mutex;
+double* g_noalloc_addr[kMaxDevices] = {};
+
+// The device address of the static workspace on the current device, looked up
+// once per device (host code cannot use the array's name as an address).
+int noalloc_workspace(double** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return FP8Z1_ECUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return FP8Z1_ECUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<double*>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return FP8Z1_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks, double* d_sumsq,
+                                       int32_t* d_found_inf, void* stream)
+{
+    if (!grad_shard || !d_sumsq || !d_found_inf || n_blocks < 0) return FP8Z1_EINVAL;
+    if (n_blocks > FP8Z1_NOALLOC_MAX_BLOCKS) return FP8Z1_EINVAL;  // beyond the static workspace
+    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    if (n_blocks == 0) return FP8Z1_OK;
+    double* partials = nullptr;
+    const int st = noalloc_workspace(&partials);
+    if (st != FP8Z1_OK) return st;
+    unsigned* counter = reinterpret_cast<unsigned*>(partials + kNoAllocMaxCtas);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the counter must start at zero; the partials are written before they are read
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned), s) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    const int64_t grid = (n_blocks + kNoAllocBlocksPerCta - 1) / kNoAllocBlocksPerCta;
+    grad_norm_kernel<<<(unsigned)grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(grad_shard),
+                                                         n_blocks, partials, counter, d_sumsq, d_found_inf);
     return fp8z1::launch_status();
 }

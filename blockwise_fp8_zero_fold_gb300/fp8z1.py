@@ -74,6 +74,7 @@ _SIGS = {
     "fp8z1_fold": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int64, C.c_int64, _P]),
     "fp8z1_unfold": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int64, C.c_int64, _P]),
     "fp8z1_grad_norm": (C.c_int, [_P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_grad_norm_noalloc": (C.c_int, [_P, C.c_int64, _P, _P, _P]),
     "fp8z1_step": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, C.c_int64,
                              C.c_int64, _P, _P, _P]),
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
@@ -218,6 +219,18 @@ def fp8z1_grad_norm(layout: Layout, grad_shard, b0: int, b1: int, d_sumsq, d_fou
                     stream=None):
     _check(lib().fp8z1_grad_norm(layout.handle, _ptr(grad_shard), int(b0), int(b1), _ptr(d_sumsq),
                                  _ptr(d_found_inf), _stream(stream)), "fp8z1_grad_norm")
+
+
+NOALLOC_MAX_BLOCKS = 262144
+
+
+def fp8z1_grad_norm_noalloc(grad_shard, n_blocks: int, d_sumsq, d_found_inf, stream=None):
+    """The grad norm of fp8z1_grad_norm for callers that cannot allocate
+    device memory: no layout, a static device workspace, at most
+    NOALLOC_MAX_BLOCKS blocks per call."""
+    _check(lib().fp8z1_grad_norm_noalloc(_ptr(grad_shard), int(n_blocks), _ptr(d_sumsq),
+                                         _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_grad_norm_noalloc")
 
 
 def make_hp(lr, beta1, beta2, eps, weight_decay, max_norm, loss_scale, step) -> fp8z1_adamw_hp:

@@ -177,6 +177,34 @@ int fp8z1_unfold(const fp8z1_layout* layout, const void* src_shard, void* const*
 int fp8z1_grad_norm(const fp8z1_layout* layout, const float* grad_shard, int64_t b0, int64_t b1,
                     double* d_sumsq, int32_t* d_found_inf, void* stream);
 
+/* ---- grad norm without any allocation ------------------------------------ */
+
+/* The pages have no counterpart to this call: it serves callers that cannot
+ * call cudaMalloc at all -- a framework whose caching allocator already owns
+ * the device memory (a foreign cudaMalloc can fail or make the driver
+ * synchronise the device), or a step loop that must never block on an
+ * allocation.  It computes what fp8z1_grad_norm computes, for the
+ * `n_blocks` blocks at `grad_shard` (pointing at block b0 of the grad buffer;
+ * n_blocks = b1 - b0), with the same kernel and the same accuracy; the
+ * summation is split differently, so the two results agree to about 1e-13
+ * relative, not bit for bit.  It needs no layout and allocates nothing: its
+ * workspace is a static device array of 4097 doubles (about 32 KB) that every
+ * device loading the library holds until the process exits.
+ *   - At most FP8Z1_NOALLOC_MAX_BLOCKS blocks per call (EINVAL beyond that);
+ *     split a larger range into several calls, which accumulate.
+ *   - The first call on each device looks up the workspace address on the
+ *     host (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one workspace, and a call leaves its contents
+ *     behind; the call clears the part that must start at zero on its
+ *     stream.  Calls that overlap on the device race: issue them on one
+ *     stream or otherwise order them.
+ * Errors: EINVAL (null, n_blocks < 0 or > FP8Z1_NOALLOC_MAX_BLOCKS), EALIGN,
+ * ECUDA. */
+#define FP8Z1_NOALLOC_MAX_BLOCKS 262144
+int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks, double* d_sumsq,
+                            int32_t* d_found_inf, void* stream);
+
 /* ---- fused step (§总结; "DeepSpeed ZeRO 优化" §三, §七) -------------------- */
 
 /* One optimizer step over blocks [b0, b1) of the shard, in one HBM pass:
