@@ -57,6 +57,21 @@ def _ncu_traffic():
         return None
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's ``x`` (the slowest rank sets the time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, seconds: float) -> float:
+    """Units processed by all ranks per second of the slowest rank."""
+    return world * units_per_rank * steps / seconds
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -186,14 +201,10 @@ def bench_ours(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
     ms_per_step = elapsed_ms / args.steps
-    value = world * n_pad * args.steps / (elapsed_ms / 1e3)
+    value = whole_job_rate(n_pad, world, args.steps, elapsed_ms / 1e3)
 
     peak, peak_kind = _peak_hbm()
     step_bytes = STEP_BYTES_PER_ELEM * n_pad + STEP_BYTES_PER_BLOCK * nblk
@@ -236,12 +247,8 @@ def bench_ours(args, rank, world, dist):
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
-        wall = time.perf_counter() - t0
-        if dist is not None:
-            t = torch.tensor([wall], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            wall = float(t.item())
-        e2e = {"value": world * n_pad * args.e2e_steps / wall, "unit": "elem/s",
+        wall = max_over_ranks(time.perf_counter() - t0, dist, dev)
+        e2e = {"value": whole_job_rate(n_pad, world, args.e2e_steps, wall), "unit": "elem/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": wall / args.e2e_steps * 1e3, "steps": args.e2e_steps}
         del hgrads, hfp8

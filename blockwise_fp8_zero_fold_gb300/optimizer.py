@@ -87,6 +87,31 @@ class ShardOptimizer:
             off += e * rb * cb
         return out
 
+    # -- checkpoint / resume --------------------------------------------------
+    def state_dict(self) -> dict:
+        """Everything a resumed run needs: the shard's folded FP32 master / m /
+        v, the codes and scales, and the host scalars (t, S, clean-step count).
+        The buffers are the 1-D block layout itself, so a reload is a copy."""
+        return {
+            "shapes": [tuple(s) for s in self.shapes], "b0": self.b0, "b1": self.b1,
+            "master": self.master.cpu(), "m": self.m.cpu(), "v": self.v.cpu(),
+            "codes": self.codes.cpu(), "scales": self.scales.cpu(), "hp": dict(self.hp),
+            "scaler": {"scale": self.scaler.scale, "step": self.scaler.step,
+                       "good_steps": self.scaler.good_steps,
+                       "growth_interval": self.scaler.growth_interval},
+        }
+
+    def load_state_dict(self, sd: dict):
+        if [tuple(s) for s in sd["shapes"]] != [tuple(s) for s in self.shapes] or \
+                (sd["b0"], sd["b1"]) != (self.b0, self.b1):
+            raise ValueError("checkpoint was taken for another layout or shard")
+        for name in ("master", "m", "v", "codes", "scales"):
+            getattr(self, name).copy_(sd[name])
+        self.hp = dict(sd["hp"])
+        sc = sd["scaler"]
+        self.scaler = F.fp8z1_loss_scaler(sc["scale"], sc["step"], sc["good_steps"],
+                                          sc["growth_interval"])
+
     # -- one step -------------------------------------------------------------
     def launch_step(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
                     stream=None):

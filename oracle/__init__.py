@@ -84,6 +84,7 @@ def lib():
             L.oracle_unfold.restype = C.c_int
             L.oracle_acc_init.argtypes = [C.POINTER(Acc)]
             L.oracle_acc_add.argtypes = [C.POINTER(Acc), P, i64]
+            L.oracle_acc_merge.argtypes = [C.POINTER(Acc), C.POINTER(Acc)]
             L.oracle_acc_result.argtypes = [C.POINTER(Acc)]
             L.oracle_acc_result.restype = C.c_double
             L.oracle_sumsq.argtypes = [P, i64, C.POINTER(C.c_double), C.POINTER(i32)]
@@ -185,12 +186,38 @@ class SumsqAccumulator:
         g = np.ascontiguousarray(g, dtype=np.float32)
         lib().oracle_acc_add(C.byref(self._a), g.ctypes.data, g.size)
 
+    def merge(self, other: "SumsqAccumulator"):
+        lib().oracle_acc_merge(C.byref(self._a), C.byref(other._a))
+
     def result(self) -> float:
         return float(lib().oracle_acc_result(C.byref(self._a)))
 
     @property
     def found_inf(self) -> int:
         return int(self._a.found_inf)
+
+
+def sumsq_parallel(arrays, threads: int = 8, chunk: int = 1 << 24):
+    """Exact sum of squares of several float32 arrays, chunks added in threads
+    (each chunk through the same single-threaded accumulator, then merged
+    exactly).  Returns (sumsq, found_inf)."""
+    from concurrent.futures import ThreadPoolExecutor
+    pieces = []
+    for a in arrays:
+        a = np.ascontiguousarray(a, dtype=np.float32).reshape(-1)
+        for i in range(0, a.size, chunk):
+            pieces.append(a[i:i + chunk])
+
+    def work(p):
+        acc = SumsqAccumulator()
+        acc.add(p)
+        return acc
+
+    total = SumsqAccumulator()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for acc in ex.map(work, pieces):
+            total.merge(acc)
+    return total.result(), total.found_inf
 
 
 def sumsq(g: np.ndarray):

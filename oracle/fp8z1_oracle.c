@@ -251,6 +251,23 @@ void oracle_acc_add(orc_sumsq_acc* a, const float* g, int64_t n)
     for (int64_t i = 0; i < n; ++i) acc_add_square(a, g[i]);
 }
 
+/* a += b, exactly (big-integer addition of the limbs; flags OR-ed): the sum
+ * of two exact partial sums is the exact sum of their terms. */
+void oracle_acc_merge(orc_sumsq_acc* a, const orc_sumsq_acc* b)
+{
+    uint64_t carry = 0;
+    for (int32_t j = 0; j < ORC_ACC_LIMBS; ++j) {
+        uint64_t s = a->limb[j] + b->limb[j];
+        uint64_t c1 = s < a->limb[j];
+        uint64_t t = s + carry;
+        uint64_t c2 = t < s;
+        a->limb[j] = t;
+        carry = c1 | c2;
+    }
+    a->found_inf |= b->found_inf;
+    a->found_nan |= b->found_nan;
+}
+
 static int acc_bit(const orc_sumsq_acc* a, int64_t i)
 {
     return (int)((a->limb[i / 64] >> (i % 64)) & 1u);

@@ -55,6 +55,18 @@ def test_sumsq_closed_forms():
     assert oracle.sumsq(np.full(1000, big, np.float32))[0] == pytest.approx(1000 * float(big) ** 2, rel=1e-15)
 
 
+def test_merge_and_parallel_equal_one_shot():
+    rng = np.random.default_rng(6)
+    parts = [(rng.standard_normal(n) * 10.0 ** rng.integers(-20, 20)).astype(np.float32)
+             for n in (1, 1000, 70001, 3)]
+    whole = np.concatenate(parts)
+    s, f = oracle.sumsq(whole)
+    assert oracle.sumsq_parallel(parts, threads=3, chunk=4096) == (s, 0)
+    assert s == _fsum_squares(whole)
+    parts[2][5] = np.nan
+    assert oracle.sumsq_parallel(parts, threads=2, chunk=4096)[1] == 1
+
+
 def test_chunked_equals_one_shot():
     rng = np.random.default_rng(5)
     g = rng.standard_normal(100003).astype(np.float32)
