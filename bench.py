@@ -154,67 +154,112 @@ def bench_ours(args, rank, world, dist):
     stream = torch.cuda.current_stream()
     n_pad, n_real, nblk = opt.n_padded, opt.n_real, opt.nblk
 
-    # warm-up
-    for _ in range(args.warmup):
-        opt.step(grads, fp8)
-    torch.cuda.synchronize()
+    def stages(path):
+        """The kernels of one step on ``path``, as (label, launch) pairs."""
+        def norm_fused():
+            opt.sumsq.zero_()
+            opt.found_inf.zero_()
+            F.fp8z1_fold_norm(opt.layout, gptrs, None, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
 
-    # timed region: K whole-path steps, per-kernel events on the launching stream
-    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)] for k in ("fold", "norm", "step", "unfold")}
+        def step_fused():
+            hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
+            F.fp8z1_step_fused(opt.layout, hp, d_grad_params=gptrs, master_shard=opt.master,
+                               m_shard=opt.m, v_shard=opt.v, d_fp8_params=fptrs,
+                               scale_shard=opt.scales, b0=opt.b0, b1=opt.b1, d_sumsq=opt.sumsq,
+                               d_found_inf=opt.found_inf)
+
+        def fold():
+            F.fp8z1_fold(opt.layout, gptrs, gbuf, 4, opt.b0, opt.b1)
+
+        def norm():
+            opt.sumsq.zero_()
+            opt.found_inf.zero_()
+            F.fp8z1_grad_norm(opt.layout, gbuf, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
+
+        def step():
+            hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
+            F.fp8z1_step(opt.layout, hp, gbuf, opt.master, opt.m, opt.v, opt.codes, opt.scales,
+                         opt.b0, opt.b1, opt.sumsq, opt.found_inf)
+
+        def unfold():
+            F.fp8z1_unfold(opt.layout, opt.codes, fptrs, 1, opt.b0, opt.b1)
+
+        if path == "fused":
+            return [("fold_norm", norm_fused), ("step", step_fused)]
+        return [("fold", fold), ("norm", norm), ("step", step), ("unfold", unfold)]
+
+    def run_steps(path, k, events=None):
+        skipped = 0
+        for i in range(k):
+            for name, fn in stages(path):
+                if events is not None:
+                    events[name][i][0].record(stream)
+                fn()
+                if events is not None:
+                    events[name][i][1].record(stream)
+            skipped += opt.finish_step()  # host reads found_inf (a10)
+        return skipped
+
+    def timed(path, k):
+        names = [n for n, _ in stages(path)]
+        ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(k)] for n in names}
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed")
+        t0.record(stream)
+        sk = run_steps(path, k, ev)
+        t1.record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+        kern = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+        return ms, kern, sk
+
+    gptrs = opt._ptrs(grads)
+    fptrs = opt._ptrs(fp8)
+    gbuf = torch.empty(opt.master.numel(), dtype=torch.float32, device=dev) if args.path == "unfused" \
+        or args.compare else None
+
+    # warm-up, then the timed region with clocks sampled during it
+    run_steps(args.path, args.warmup)
+    torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.nvtx.range_push("timed")
-    t_start.record(stream)
-    skipped = 0
-    for i in range(args.steps):
-        e = ev["fold"][i]
-        e[0].record(stream)
-        opt.fold_into(grads, opt.grad)
-        e[1].record(stream)
-        opt.sumsq.zero_()
-        opt.found_inf.zero_()
-        e = ev["norm"][i]
-        e[0].record(stream)
-        F.fp8z1_grad_norm(opt.layout, opt.grad, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
-        e[1].record(stream)
-        hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
-        e = ev["step"][i]
-        e[0].record(stream)
-        F.fp8z1_step(opt.layout, hp, opt.grad, opt.master, opt.m, opt.v, opt.codes, opt.scales,
-                     opt.b0, opt.b1, opt.sumsq, opt.found_inf)
-        e[1].record(stream)
-        e = ev["unfold"][i]
-        e[0].record(stream)
-        opt.unfold_from(opt.codes, fp8)
-        e[1].record(stream)
-        skipped += opt.finish_step()  # host reads found_inf (a10)
-    t_end.record(stream)
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    elapsed_ms, kern, skipped = timed(args.path, args.steps)
     clk = clocks.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
-    kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(n_pad, world, args.steps, elapsed_ms / 1e3)
+    other = None
+    if args.compare:
+        alt = "unfused" if args.path == "fused" else "fused"
+        run_steps(alt, 2)
+        a_ms, a_kern, _ = timed(alt, max(3, args.steps // 4))
+        other = {"path": alt, "ms_per_step": a_ms / max(3, args.steps // 4), "kernels_ms": a_kern}
+    if gbuf is not None:
+        del gbuf
 
     peak, peak_kind = _peak_hbm()
-    step_bytes = STEP_BYTES_PER_ELEM * n_pad + STEP_BYTES_PER_BLOCK * nblk
+    # algorithmic bytes of the dominant kernel (the fused step): grads read on
+    # the real elements (row-major) or the padded ones (folded), master/m/v read
+    # and written (24 B), one code byte per real (row-major) or padded element
+    if args.path == "fused":
+        step_bytes = 4 * n_real + 24 * n_pad + 1 * n_real + STEP_BYTES_PER_BLOCK * nblk
+        gbs = {"fold_norm": 4 * n_real / kern["fold_norm"] / 1e6}
+    else:
+        step_bytes = STEP_BYTES_PER_ELEM * n_pad + STEP_BYTES_PER_BLOCK * nblk
+        gbs = {"fold": 4 * (n_real + n_pad) / kern["fold"] / 1e6, "norm": 4 * n_pad / kern["norm"] / 1e6,
+               "unfold": 1 * (n_real + n_pad) / kern["unfold"] / 1e6}
     achieved = step_bytes / (kern["step"] / 1e3) / 1e9
-    fold_bytes = 4 * (n_real + n_pad)
-    unfold_bytes = 1 * (n_real + n_pad)
-    norm_bytes = 4 * n_pad
+    gbs["step"] = achieved
     tr = _ncu_traffic()
     traffic = None
-    if tr and tr.get("workload") == args.workload and tr.get("source_sha") == _step_source_sha():
+    if tr and tr.get("workload") == args.workload and tr.get("path") == args.path and \
+            tr.get("source_sha") == _step_source_sha() and not args.experts:
         traffic = tr.get("bytes_per_launch")
 
     # e2e: the same step through the public API, grads from pinned host memory
@@ -273,14 +318,16 @@ def bench_ours(args, rank, world, dist):
             "l2": "inputs larger than L2 (~31 GB resident per step), no flush",
             "value_counts": "padded elements per second through the whole step",
         },
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (3 if args.path == "fused" else 4) * args.steps,
+        "path": args.path,
         "kernels_ms": kern,
-        "kernels_gbs": {"fold": fold_bytes / kern["fold"] / 1e6, "norm": norm_bytes / kern["norm"] / 1e6,
-                        "step": achieved, "unfold": unfold_bytes / kern["unfold"] / 1e6},
+        "kernels_gbs": gbs,
+        "other_path": other,
         "step_kernel_elem_per_s": n_pad / (kern["step"] / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fp8z1_step", "peak_source": peak_kind,
+                     "kernel": "fp8z1_step_fused" if args.path == "fused" else "fp8z1_step",
+                     "peak_source": peak_kind,
                      "bytes_per_launch": step_bytes},
         "clocks": clk,
         "skipped_steps": skipped,
@@ -381,6 +428,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="moe")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+                    help="fused: norm from row-major grads + step with fused fold/unfold (2 passes); "
+                         "unfused: fold, norm, step, unfold (4 passes)")
+    ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=3)

@@ -1,10 +1,14 @@
 // Global grad norm: the sum of squares of the loss-scaled FP32 grads of a
-// block range, plus the inf/nan flag.
+// block range, plus the inf/nan flag -- read from the folded grad shard
+// (fp8z1_grad_norm) or straight from the row-major grads through the block
+// lookup table, optionally storing the folded blocks on the way
+// (fp8z1_fold_norm: the fold of the grads fused with the norm).
 //
 // "DeepSpeed ZeRO 优化" §七 梯度裁剪: the global norm is the square root of the
 // sum over every rank of its partial sum of squares (an all-reduce); the clip
 // coefficient is formed from it.  §六 / §九 Q6: an inf or nan among the grads
-// skips the step.
+// skips the step.  "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结 /
+// §参数布局变换: the reduced grads are folded into the optimizer's layout.
 //
 // Accuracy: each square is split exactly into float hi + lo parts
 // (x*x and fma(x, x, -x*x)), and a thread adds its 32 squares of a block with
@@ -12,14 +16,20 @@
 // the exact value; partials are then summed in double.  The result is well
 // inside 1e-12 relative of the exact sum -- close enough that the clip
 // coefficient formed from it rounds to the same FP32 number as one formed from
-// the exact sum, except in rare ties.  A thread whose 32 values hold one with
-// |x| outside [2^-60, 2^60) (or an inf/nan) redoes them in double, where the
-// squares of any finite float are exact.
+// the exact sum, except in rare ties.  The float path is exact enough only
+// while the partial stays in [2^-90, 2^100), or is 0 because every value is 0:
+// an inf or nan, a square that overflows, or tiny values (whose squares
+// underflow, possibly to a partial of 0) land outside, and then the thread
+// redoes those 32 values in double, where the square of any float is exact.
 //
-// Reduction: a fixed number of CTAs each take a contiguous run of blocks;
-// each writes one double to a workspace, and the last CTA to finish (an atomic
-// ticket, no waiting) adds the partials in a fixed order.  The result is
-// deterministic for a given device and range.
+// Latency: a persistent CTA per SM walks a contiguous run of blocks; each
+// thread loads the next block's 32 values (and, reading row-major, looks up
+// the block after that in the table) while it sums the current ones, so a
+// CTA always has a block's worth of loads in flight.
+//
+// Reduction: each CTA writes one double to a workspace, and the last CTA to
+// finish (an atomic ticket, no waiting) adds the partials in a fixed order.
+// The result is deterministic for a given device and range.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,7 +39,7 @@
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kVecPerThread = FP8Z1_BLOCK_ELEMS / 4 / kThreads;  // 8 float4
+constexpr int kVec = FP8Z1_BLOCK_ELEMS / 4 / kThreads;  // 8 float4 per thread and block
 constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& err)
@@ -40,23 +50,21 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& err)
     err = __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb));
 }
 
-// true when x is an inf/nan or too small/large for the float fast path
-__device__ __forceinline__ bool out_of_fast_range(float x)
+__device__ __forceinline__ void add_square(float x, float& hi, float& lo, unsigned& nz)
 {
-    const unsigned u = __float_as_uint(x) & 0x7fffffffu;
-    constexpr unsigned kLo = 0x21800000u;  // 2^-60
-    constexpr unsigned kHi = 0x5d800000u;  // 2^60
-    return u != 0u && (u - kLo) >= (kHi - kLo);
-}
-
-__device__ __forceinline__ void add_square(float x, float& hi, float& lo, bool& slow)
-{
-    slow |= out_of_fast_range(x);
+    nz |= __float_as_uint(x) & 0x7fffffffu;  // any nonzero magnitude
     const float sq = __fmul_rn(x, x);
-    const float e = __fmaf_rn(x, x, -sq);  // x*x = sq + e exactly (in range)
+    const float e = __fmaf_rn(x, x, -sq);  // x*x = sq + e exactly (no under/overflow)
     float t;
     two_sum(hi, sq, hi, t);
     lo = __fadd_rn(lo, __fadd_rn(t, e));
+}
+
+// The float partial is exact enough when it lies in [2^-90, 2^100), or when
+// every value was zero (nz == 0).
+__device__ __forceinline__ bool float_path_ok(float hi, unsigned nz)
+{
+    return hi < 0x1p100f && (hi >= 0x1p-90f || nz == 0u);
 }
 
 __device__ __forceinline__ void add_square_exact(float x, double& acc, int& bad)
@@ -74,47 +82,162 @@ __device__ __forceinline__ double warp_sum(double v)
     return v;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) grad_norm_kernel(const float4* __restrict__ g,
-                                                             int64_t nblocks,
-                                                             double* __restrict__ partials,
-                                                             unsigned* __restrict__ counter,
-                                                             double* __restrict__ d_sumsq,
-                                                             int32_t* __restrict__ d_found_inf)
+__device__ __forceinline__ void sum_block(const float4 (&x)[kVec], double& acc, int& bad)
+{
+    float hi = 0.0f, lo = 0.0f;
+    unsigned nz = 0u;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        add_square(x[j].x, hi, lo, nz);
+        add_square(x[j].y, hi, lo, nz);
+        add_square(x[j].z, hi, lo, nz);
+        add_square(x[j].w, hi, lo, nz);
+    }
+    if (float_path_ok(hi, nz)) {
+        acc += (double)hi;
+        acc += (double)lo;
+    } else {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            add_square_exact(x[j].x, acc, bad);
+            add_square_exact(x[j].y, acc, bad);
+            add_square_exact(x[j].z, acc, bad);
+            add_square_exact(x[j].w, acc, bad);
+        }
+    }
+}
+
+// Where block k's grads live in the row-major params.
+struct RowSrc {
+    const float* tile;
+    int64_t ld;
+    int rows, cols;
+    bool vec;  // 16-byte loads (ld % 4 == 0 and an aligned tile)
+    bool bad;  // null or misaligned param pointer
+};
+
+__device__ __forceinline__ RowSrc row_src(const fp8z1_block* __restrict__ lut,
+                                          const float* const* __restrict__ params, int64_t k)
+{
+    const fp8z1_block blk = lut[k];
+    const float* base = params[blk.param];
+    RowSrc s;
+    s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
+    s.tile = s.bad ? nullptr : base + blk.src_offset;
+    s.ld = blk.ld;
+    s.rows = blk.rows_real;
+    s.cols = blk.cols_real;
+    s.vec = !s.bad && (blk.ld & 3) == 0 && (reinterpret_cast<uintptr_t>(s.tile) & 15) == 0;
+    return s;
+}
+
+struct NormArgs {
+    const float4* g;              // folded grads at block b0 (!ROWS)
+    const fp8z1_block* lut;       // ROWS
+    const float* const* params;   // ROWS: row-major FP32 grads
+    float4* store;                // STORE: folded grads at block b0
+    int64_t b0;                   // first block (ROWS: LUT index)
+    int64_t nblocks;
+    double* partials;             // one per CTA
+    unsigned* counter;
+    unsigned* status;
+    double* sumsq;
+    int32_t* found_inf;
+};
+
+// Issue the loads of block k (index from b0): this thread's 32 values.  Chunk
+// j is tid + 512 j: block row (tid + 512 j) / 32, columns 4 * ((tid + 512 j)
+// % 32) .. + 3.  Zeros outside the real extent.
+template <bool ROWS>
+__device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
+                                           float4 (&x)[kVec])
+{
+    if (!ROWS) {
+        const float4* p = a.g + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        const int ci = tid + j * kThreads;
+        const int r = ci >> 5, c = (ci & 31) << 2;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!s.bad && r < s.rows) {
+            const float* src = s.tile + r * s.ld + c;
+            if (s.vec) {  // a 4-column group is then all real or all padding
+                if (c < s.cols) v = __ldcs(reinterpret_cast<const float4*>(src));
+            } else {
+                if (c + 0 < s.cols) v.x = __ldcs(src + 0);
+                if (c + 1 < s.cols) v.y = __ldcs(src + 1);
+                if (c + 2 < s.cols) v.z = __ldcs(src + 2);
+                if (c + 3 < s.cols) v.w = __ldcs(src + 3);
+            }
+        }
+        x[j] = v;
+    }
+}
+
+template <bool ROWS>
+__device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t k)
+{
+    if (ROWS) return row_src(a.lut, a.params, a.b0 + k);
+    return RowSrc{};
+}
+
+// Sum (and store) block k, whose values are in x.
+template <bool ROWS, bool STORE>
+__device__ __forceinline__ void finish_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
+                                             const float4 (&x)[kVec], double& acc, int& bad)
+{
+    if (ROWS && s.bad) {  // unreadable grads: nothing is summed or stored
+        if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
+        bad = 1;          // raise found_inf so the step is skipped
+        return;
+    }
+    if (STORE) {
+        float4* dst = a.store + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) __stcs(dst + j * kThreads, x[j]);
+    }
+    sum_block(x, acc, bad);
+}
+
+template <bool ROWS, bool STORE>
+__global__ void __launch_bounds__(kThreads, 1) norm_kernel(const NormArgs a)
 {
     __shared__ double s_part[kWarps];
     __shared__ int s_last;
     const int tid = threadIdx.x;
-    const int64_t k0 = (int64_t)blockIdx.x * nblocks / gridDim.x;
-    const int64_t k1 = (int64_t)(blockIdx.x + 1) * nblocks / gridDim.x;
+    const int64_t k0 = (int64_t)blockIdx.x * a.nblocks / gridDim.x;
+    const int64_t k1 = (int64_t)(blockIdx.x + 1) * a.nblocks / gridDim.x;
 
     double acc = 0.0;
     int bad = 0;
-    for (int64_t k = k0; k < k1; ++k) {
-        const float4* p = g + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
-        float4 x[kVecPerThread];
-#pragma unroll
-        for (int j = 0; j < kVecPerThread; ++j) x[j] = __ldcs(p + j * kThreads);
-        float hi = 0.0f, lo = 0.0f;
-        bool slow = false;
-#pragma unroll
-        for (int j = 0; j < kVecPerThread; ++j) {
-            add_square(x[j].x, hi, lo, slow);
-            add_square(x[j].y, hi, lo, slow);
-            add_square(x[j].z, hi, lo, slow);
-            add_square(x[j].w, hi, lo, slow);
-        }
-        if (!slow) {
-            acc += (double)hi;
-            acc += (double)lo;
-        } else {
-#pragma unroll
-            for (int j = 0; j < kVecPerThread; ++j) {
-                add_square_exact(x[j].x, acc, bad);
-                add_square_exact(x[j].y, acc, bad);
-                add_square_exact(x[j].z, acc, bad);
-                add_square_exact(x[j].w, acc, bad);
-            }
-        }
+    // Two register buffers.  Loop invariant at the head: xa holds block k
+    // (loads issued), sa = where block k lives, sb = where block k+1 lives.
+    float4 xa[kVec], xb[kVec];
+    RowSrc sa = {}, sb = {};
+    int64_t k = k0;
+    if (k < k1) {
+        sa = src_of<ROWS>(a, k);
+        load_block<ROWS>(a, sa, k, tid, xa);
+        if (k + 1 < k1) sb = src_of<ROWS>(a, k + 1);
+    }
+    while (k < k1) {
+        if (k + 1 < k1) load_block<ROWS>(a, sb, k + 1, tid, xb);
+        RowSrc sc = {};
+        if (k + 2 < k1) sc = src_of<ROWS>(a, k + 2);
+        finish_block<ROWS, STORE>(a, sa, k, tid, xa, acc, bad);
+        if (++k >= k1) break;
+        // xb holds block k, sb = where it lives, sc = where block k+1 lives
+        if (k + 1 < k1) load_block<ROWS>(a, sc, k + 1, tid, xa);
+        RowSrc sd = {};
+        if (k + 2 < k1) sd = src_of<ROWS>(a, k + 2);
+        finish_block<ROWS, STORE>(a, sb, k, tid, xb, acc, bad);
+        ++k;
+        sa = sc;
+        sb = sd;
     }
 
     // CTA sum in a fixed order
@@ -124,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 2) grad_norm_kernel(const float4* __
     if (tid == 0) {
         double t = 0.0;
         for (int w = 0; w < kWarps; ++w) t += s_part[w];
-        partials[blockIdx.x] = t;
-        if (bad) atomicOr(d_found_inf, 1);
+        a.partials[blockIdx.x] = t;
+        if (bad) atomicOr(a.found_inf, 1);
         __threadfence();
-        const unsigned ticket = atomicAdd(counter, 1u);
+        const unsigned ticket = atomicAdd(a.counter, 1u);
         s_last = (ticket == gridDim.x - 1);
     }
     __syncthreads();
@@ -136,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 2) grad_norm_kernel(const float4* __
     // the last CTA: add the partials of every CTA in a fixed order
     __threadfence();
     double t = 0.0;
-    for (int i = tid; i < (int)gridDim.x; i += kThreads) t += __ldcg(partials + i);
+    for (int i = tid; i < (int)gridDim.x; i += kThreads) t += __ldcg(a.partials + i);
     t = warp_sum(t);
     __syncthreads();  // s_part reuse
     if ((tid & 31) == 0) s_part[tid >> 5] = t;
@@ -144,9 +267,18 @@ __global__ void __launch_bounds__(kThreads, 2) grad_norm_kernel(const float4* __
     if (tid == 0) {
         double total = 0.0;
         for (int w = 0; w < kWarps; ++w) total += s_part[w];
-        *d_sumsq = *d_sumsq + total;
-        *counter = 0u;  // ready for the next launch on this layout
+        *a.sumsq = *a.sumsq + total;
+        *a.counter = 0u;  // ready for the next launch on this workspace
     }
+}
+
+// one CTA of 512 threads per SM, at most one per block and one per partial slot
+int64_t persistent_grid(const fp8z1_layout* L, int64_t n)
+{
+    int64_t grid = (int64_t)L->sm_count;
+    if (grid > n) grid = n;
+    if (grid > L->max_partials) grid = L->max_partials;
+    return grid;
 }
 
 }  // namespace
@@ -161,12 +293,48 @@ extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, i
         return FP8Z1_EALIGN;
     const int64_t n = b1 - b0;
     if (n == 0) return FP8Z1_OK;
-    // two CTAs of 512 threads per SM, at most one per block and one per partial slot
-    int64_t grid = (int64_t)L->sm_count * 2;
-    if (grid > n) grid = n;
-    if (grid > L->max_partials) grid = L->max_partials;
-    grad_norm_kernel<<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4*>(grad_shard), n, L->d_partials, L->d_counter, d_sumsq, d_found_inf);
+    NormArgs a = {};
+    a.g = reinterpret_cast<const float4*>(grad_shard);
+    a.b0 = b0;
+    a.nblocks = n;
+    a.partials = L->d_partials;
+    a.counter = L->d_counter;
+    a.status = L->d_status;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    norm_kernel<false, false><<<(unsigned)persistent_grid(L, n), kThreads, 0,
+                                 static_cast<cudaStream_t>(stream)>>>(a);
+    return fp8z1::launch_status();
+}
+
+extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad_params, float* grad_shard,
+                               int64_t b0, int64_t b1, double* d_sumsq, int32_t* d_found_inf, void* stream)
+{
+    if (!d_grad_params || !d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
+    const int st = fp8z1::check_range(L, b0, b1);
+    if (st != FP8Z1_OK) return st;
+    if (!fp8z1::aligned(d_grad_params, sizeof(void*)) || (grad_shard && !fp8z1::aligned(grad_shard, 16)) ||
+        !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    const int64_t n = b1 - b0;
+    if (n == 0) return FP8Z1_OK;
+    NormArgs a = {};
+    a.lut = L->d_lut;
+    a.params = d_grad_params;
+    a.store = reinterpret_cast<float4*>(grad_shard);
+    a.b0 = b0;
+    a.nblocks = n;
+    a.partials = L->d_partials;
+    a.counter = L->d_counter;
+    a.status = L->d_status;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    const unsigned grid = (unsigned)persistent_grid(L, n);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (grad_shard)
+        norm_kernel<true, true><<<grid, kThreads, 0, s>>>(a);
+    else
+        norm_kernel<true, false><<<grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();
 }
 
@@ -240,8 +408,14 @@ extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks
         cudaGetLastError();
         return FP8Z1_ECUDA;
     }
+    NormArgs a = {};
+    a.g = reinterpret_cast<const float4*>(grad_shard);
+    a.nblocks = n_blocks;
+    a.partials = partials;
+    a.counter = counter;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
     const int64_t grid = (n_blocks + kNoAllocBlocksPerCta - 1) / kNoAllocBlocksPerCta;
-    grad_norm_kernel<<<(unsigned)grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(grad_shard),
-                                                         n_blocks, partials, counter, d_sumsq, d_found_inf);
+    norm_kernel<false, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();
 }

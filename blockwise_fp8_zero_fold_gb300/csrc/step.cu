@@ -5,16 +5,26 @@
 // "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结: the optimizer update is
 // elementwise on the rank's slice, and each rank then quantises new FP8 params
 // and their scales from its FP32 master; §Blockwise 量化: one scale per
-// 128x128 block.  "DeepSpeed ZeRO 优化" §三: unscale and clip, then the
-// update, then the low-precision copy; §七: clip_coef = max_norm /
+// 128x128 block; §参数布局变换: grads are folded to the optimizer's layout and
+// the FP8 params unfolded back.  "DeepSpeed ZeRO 优化" §三: unscale and clip,
+// then the update, then the low-precision copy; §七: clip_coef = max_norm /
 // (||g_s|| / S + 1e-6), applied when < 1; §六: a found inf skips the step.
 //
 // One CTA of 512 threads per block of 16384 elements; thread t owns the
-// float4 chunks t, t+512, ..., t+3584 of the block.  It streams grad / master
-// / m / v in, updates them, writes master / m / v back at once and keeps its
-// 32 new master values in registers while the CTA reduces the block amax
-// (warp shuffles, then 16 partials in shared memory).  The codes are then
-// produced from the registers: no second pass over HBM.
+// float4 chunks t, t+512, ..., t+3584 of the block (chunk i is row i/32,
+// columns 4*(i%32) .. +3 of the 128x128 block, so a warp covers one block row).
+// It streams grad / master / m / v in, updates them, writes master / m / v back
+// at once and keeps its 32 new master values in registers while the CTA
+// reduces the block amax (warp shuffles, then 16 partials in shared memory).
+// The codes are then produced from the registers: no second pass over HBM.
+//
+// Where the grads come from and where the codes go is chosen at compile time:
+//   GRAD_ROWS    grads are read from the row-major params through the block
+//                lookup table (the fold of the grads, fused), else from the
+//                folded grad shard;
+//   CODES_ROWS   codes are written into the row-major FP8 params through the
+//                lookup table (the unfold of the codes, fused);
+//   CODES_FOLDED codes are written to the folded code shard.
 //
 // FP32 operation order per element (no contraction beyond the explicit fmas;
 // division and square root correctly rounded):
@@ -36,6 +46,23 @@ constexpr int kWarps = kThreads / 32;
 
 struct StepScalars {
     float beta1, beta2, omb1, omb2, eps, step_size, inv_sqrt_bc2, decay, max_norm, loss_scale;
+};
+
+struct StepArgs {
+    const float4* grad;          // folded grad shard (!GRAD_ROWS)
+    float4* master;
+    float4* mom1;
+    float4* mom2;
+    uint32_t* codes;             // folded code shard (CODES_FOLDED)
+    float* scales;
+    const double* sumsq;
+    const int32_t* found_inf;
+    const fp8z1_block* lut;      // GRAD_ROWS / CODES_ROWS
+    int64_t b0;
+    const float* const* grad_params;  // GRAD_ROWS: row-major FP32 grads
+    uint8_t* const* code_params;      // CODES_ROWS: row-major FP8 params
+    unsigned* status;
+    StepScalars c;
 };
 
 __device__ __forceinline__ void adamw(float gs, const StepScalars& c, float g_s, float& p, float& m,
@@ -64,25 +91,86 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(const float4* __restrict__ grad,
-                                                           float4* __restrict__ master,
-                                                           float4* __restrict__ mom1,
-                                                           float4* __restrict__ mom2,
-                                                           uint32_t* __restrict__ codes,
-                                                           float* __restrict__ scales,
-                                                           const double* __restrict__ d_sumsq,
-                                                           const int32_t* __restrict__ d_found_inf,
-                                                           StepScalars c)
+// the 4 grads of chunk (r, c) of a row-major tile; zeros outside the real extent
+__device__ __forceinline__ float4 load_grad_rows(const float* tile, int64_t ld, int r, int c, int rows,
+                                                 int cols, bool vec)
 {
-    if (*d_found_inf != 0) return;  // skipped step: write nothing
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows) {
+        const float* src = tile + r * ld + c;
+        if (vec) {  // ld % 4 == 0: a 4-column group is all real or all padding
+            if (c < cols) g = __ldcs(reinterpret_cast<const float4*>(src));
+        } else {
+            if (c + 0 < cols) g.x = __ldcs(src + 0);
+            if (c + 1 < cols) g.y = __ldcs(src + 1);
+            if (c + 2 < cols) g.z = __ldcs(src + 2);
+            if (c + 3 < cols) g.w = __ldcs(src + 3);
+        }
+    }
+    return g;
+}
+
+__device__ __forceinline__ void store_codes_rows(uint8_t* tile, int64_t ld, int r, int c, int rows,
+                                                 int cols, bool vec, uint32_t q)
+{
+    if (r >= rows) return;
+    uint8_t* dst = tile + r * ld + c;
+    if (vec) {
+        if (c < cols) __stcs(reinterpret_cast<unsigned int*>(dst), q);
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (c + b < cols) dst[b] = (uint8_t)(q >> (8 * b));
+    }
+}
+
+template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
+{
+    if (*a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
     const int tid = threadIdx.x;
     if (tid == 0) {
-        const double global = sqrt(*d_sumsq) / (double)c.loss_scale;
-        const double coef = (double)c.max_norm / (global + 1e-6);
+        const double global = sqrt(*a.sumsq) / (double)a.c.loss_scale;
+        const double coef = (double)a.c.max_norm / (global + 1e-6);
         const float clip = coef < 1.0 ? (float)coef : 1.0f;
-        s_gscale = __fdiv_rn(clip, c.loss_scale);
+        s_gscale = __fdiv_rn(clip, a.c.loss_scale);
+    }
+
+    // the block's place in its row-major param (only for the row-major forms)
+    int rows = 0, cols = 0;
+    int64_t ld = 0, off = 0;
+    int param = 0;
+    if (GRAD_ROWS || CODES_ROWS) {
+        const fp8z1_block blk = a.lut[a.b0 + blockIdx.x];
+        rows = blk.rows_real;
+        cols = blk.cols_real;
+        ld = blk.ld;
+        off = blk.src_offset;
+        param = blk.param;
+    }
+    const float* gtile = nullptr;
+    bool gvec = false;
+    if (GRAD_ROWS) {
+        const float* base = a.grad_params[param];
+        if (base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0) {
+            if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
+            return;  // uniform: the block is left untouched
+        }
+        gtile = base + off;
+        gvec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(gtile) & 15) == 0);
+    }
+    uint8_t* ctile = nullptr;
+    bool cvec = false;
+    if (CODES_ROWS) {
+        uint8_t* base = a.code_params[param];
+        if (base == nullptr) {
+            if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
+            return;
+        }
+        ctile = base + off;
+        cvec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(ctile) & 3) == 0);
     }
     __syncthreads();
     const float gs = s_gscale;
@@ -93,17 +181,23 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const float4* __restr
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         const int64_t i = base + j * kThreads;
-        const float4 g4 = __ldcs(grad + i);
-        float4 p4 = master[i];
-        float4 m4 = mom1[i];
-        float4 v4 = mom2[i];
-        adamw(gs, c, g4.x, p4.x, m4.x, v4.x);
-        adamw(gs, c, g4.y, p4.y, m4.y, v4.y);
-        adamw(gs, c, g4.z, p4.z, m4.z, v4.z);
-        adamw(gs, c, g4.w, p4.w, m4.w, v4.w);
-        __stcs(mom1 + i, m4);
-        __stcs(mom2 + i, v4);
-        __stcs(master + i, p4);
+        float4 g4;
+        if (GRAD_ROWS) {
+            const int ci = tid + j * kThreads;  // chunk index inside the block
+            g4 = load_grad_rows(gtile, ld, ci >> 5, (ci & 31) << 2, rows, cols, gvec);
+        } else {
+            g4 = __ldcs(a.grad + i);
+        }
+        float4 p4 = a.master[i];
+        float4 m4 = a.mom1[i];
+        float4 v4 = a.mom2[i];
+        adamw(gs, a.c, g4.x, p4.x, m4.x, v4.x);
+        adamw(gs, a.c, g4.y, p4.y, m4.y, v4.y);
+        adamw(gs, a.c, g4.z, p4.z, m4.z, v4.z);
+        adamw(gs, a.c, g4.w, p4.w, m4.w, v4.w);
+        __stcs(a.mom1 + i, m4);
+        __stcs(a.mom2 + i, v4);
+        __stcs(a.master + i, p4);
         pn[4 * j + 0] = p4.x;
         pn[4 * j + 1] = p4.y;
         pn[4 * j + 2] = p4.z;
@@ -118,13 +212,18 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const float4* __restr
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) bmax = fmaxf(bmax, s_amax[w]);
     const float scale = bmax == 0.0f ? 1.0f : __fdiv_rn(bmax, 448.0f);
-    if (tid == 0) scales[blockIdx.x] = scale;
+    if (tid == 0) a.scales[blockIdx.x] = scale;
 
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         const uint32_t lo = e4m3x2(__fdiv_rn(pn[4 * j + 0], scale), __fdiv_rn(pn[4 * j + 1], scale));
         const uint32_t hi = e4m3x2(__fdiv_rn(pn[4 * j + 2], scale), __fdiv_rn(pn[4 * j + 3], scale));
-        __stcs(codes + base + j * kThreads, lo | (hi << 16));
+        const uint32_t q = lo | (hi << 16);
+        if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
+        if (CODES_ROWS) {
+            const int ci = tid + j * kThreads;
+            store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
+        }
     }
 }
 
@@ -136,26 +235,9 @@ bool in_domain(const fp8z1_adamw_hp* hp)
            isfinite(hp->lr) && isfinite(hp->eps) && isfinite(hp->weight_decay);
 }
 
-}  // namespace
-
-extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
-                          float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
-                          float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
-                          const int32_t* d_found_inf, void* stream)
+// per-step scalars, in double on the host, rounded once to FP32
+StepScalars scalars(const fp8z1_adamw_hp* hp)
 {
-    if (!hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
-        !d_sumsq || !d_found_inf || !in_domain(hp))
-        return FP8Z1_EINVAL;
-    const int st = fp8z1::check_range(L, b0, b1);
-    if (st != FP8Z1_OK) return st;
-    if (b1 - b0 > 0x7fffffffLL) return FP8Z1_EINVAL;
-    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(master_shard, 16) ||
-        !fp8z1::aligned(m_shard, 16) || !fp8z1::aligned(v_shard, 16) || !fp8z1::aligned(fp8_shard, 16) ||
-        !fp8z1::aligned(scale_shard, 4) || !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
-        return FP8Z1_EALIGN;
-    if (b0 == b1) return FP8Z1_OK;
-
-    // per-step scalars, in double on the host, rounded once to FP32
     const double t = (double)hp->step;
     const double bc1 = 1.0 - pow((double)hp->beta1, t);
     const double bc2 = 1.0 - pow((double)hp->beta2, t);
@@ -170,10 +252,101 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
     c.decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);
     c.max_norm = hp->max_norm;
     c.loss_scale = hp->loss_scale;
+    return c;
+}
 
-    step_kernel<<<(unsigned)(b1 - b0), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const float4*>(grad_shard), reinterpret_cast<float4*>(master_shard),
-        reinterpret_cast<float4*>(m_shard), reinterpret_cast<float4*>(v_shard),
-        reinterpret_cast<uint32_t*>(fp8_shard), scale_shard, d_sumsq, d_found_inf, c);
+int check_common(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* master, const float* m,
+                 const float* v, const float* scales, int64_t b0, int64_t b1, const double* d_sumsq,
+                 const int32_t* d_found_inf)
+{
+    if (!hp || !master || !m || !v || !scales || !d_sumsq || !d_found_inf || !in_domain(hp))
+        return FP8Z1_EINVAL;
+    const int st = fp8z1::check_range(L, b0, b1);
+    if (st != FP8Z1_OK) return st;
+    if (b1 - b0 > 0x7fffffffLL) return FP8Z1_EINVAL;
+    if (!fp8z1::aligned(master, 16) || !fp8z1::aligned(m, 16) || !fp8z1::aligned(v, 16) ||
+        !fp8z1::aligned(scales, 4) || !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    return FP8Z1_OK;
+}
+
+template <bool GR, bool CR, bool CF>
+void launch(const StepArgs& a, int64_t nb, cudaStream_t s)
+{
+    step_kernel<GR, CR, CF><<<(unsigned)nb, kThreads, 0, s>>>(a);
+}
+
+}  // namespace
+
+extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                          float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                          float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
+                          const int32_t* d_found_inf, void* stream)
+{
+    int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
+    if (st != FP8Z1_OK) return st;
+    if (!grad_shard || !fp8_shard) return FP8Z1_EINVAL;
+    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(fp8_shard, 16)) return FP8Z1_EALIGN;
+    if (b0 == b1) return FP8Z1_OK;
+    StepArgs a = {};
+    a.grad = reinterpret_cast<const float4*>(grad_shard);
+    a.master = reinterpret_cast<float4*>(master_shard);
+    a.mom1 = reinterpret_cast<float4*>(m_shard);
+    a.mom2 = reinterpret_cast<float4*>(v_shard);
+    a.codes = reinterpret_cast<uint32_t*>(fp8_shard);
+    a.scales = scale_shard;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    a.lut = L->d_lut;
+    a.b0 = b0;
+    a.status = L->d_status;
+    a.c = scalars(hp);
+    launch<false, false, true>(a, b1 - b0, static_cast<cudaStream_t>(stream));
+    return fp8z1::launch_status();
+}
+
+extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                                const float* const* d_grad_params, float* master_shard, float* m_shard,
+                                float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
+                                float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
+                                const int32_t* d_found_inf, void* stream)
+{
+    int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
+    if (st != FP8Z1_OK) return st;
+    // exactly one grad source, at least one code destination
+    if ((grad_shard == nullptr) == (d_grad_params == nullptr)) return FP8Z1_EINVAL;
+    if (fp8_shard == nullptr && d_fp8_params == nullptr) return FP8Z1_EINVAL;
+    if ((grad_shard && !fp8z1::aligned(grad_shard, 16)) || (fp8_shard && !fp8z1::aligned(fp8_shard, 16)) ||
+        (d_grad_params && !fp8z1::aligned(d_grad_params, sizeof(void*))) ||
+        (d_fp8_params && !fp8z1::aligned(d_fp8_params, sizeof(void*))))
+        return FP8Z1_EALIGN;
+    if (b0 == b1) return FP8Z1_OK;
+    StepArgs a = {};
+    a.grad = reinterpret_cast<const float4*>(grad_shard);
+    a.master = reinterpret_cast<float4*>(master_shard);
+    a.mom1 = reinterpret_cast<float4*>(m_shard);
+    a.mom2 = reinterpret_cast<float4*>(v_shard);
+    a.codes = reinterpret_cast<uint32_t*>(fp8_shard);
+    a.scales = scale_shard;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    a.lut = L->d_lut;
+    a.b0 = b0;
+    a.grad_params = d_grad_params;
+    a.code_params = d_fp8_params;
+    a.status = L->d_status;
+    a.c = scalars(hp);
+    const int64_t nb = b1 - b0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool gr = d_grad_params != nullptr, cr = d_fp8_params != nullptr, cf = fp8_shard != nullptr;
+    if (gr) {
+        if (cr && cf) launch<true, true, true>(a, nb, s);
+        else if (cr) launch<true, true, false>(a, nb, s);
+        else launch<true, false, true>(a, nb, s);
+    } else {
+        if (cr && cf) launch<false, true, true>(a, nb, s);
+        else if (cr) launch<false, true, false>(a, nb, s);
+        else launch<false, false, true>(a, nb, s);
+    }
     return fp8z1::launch_status();
 }

@@ -77,6 +77,9 @@ _SIGS = {
     "fp8z1_grad_norm_noalloc": (C.c_int, [_P, C.c_int64, _P, _P, _P]),
     "fp8z1_step": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, C.c_int64,
                              C.c_int64, _P, _P, _P]),
+    "fp8z1_fold_norm": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_step_fused": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, _P, _P,
+                                   C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
@@ -243,6 +246,26 @@ def fp8z1_step(layout: Layout, hp: fp8z1_adamw_hp, grad_shard, master_shard, m_s
                             _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard), _ptr(scale_shard),
                             int(b0), int(b1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_step")
+
+
+def fp8z1_fold_norm(layout: Layout, d_grad_params, grad_shard, b0: int, b1: int, d_sumsq,
+                    d_found_inf, stream=None):
+    """Fold (when grad_shard is not None) fused with the grad norm."""
+    _check(lib().fp8z1_fold_norm(layout.handle, _ptr(d_grad_params), _ptr(grad_shard), int(b0),
+                                 int(b1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_fold_norm")
+
+
+def fp8z1_step_fused(layout: Layout, hp: fp8z1_adamw_hp, *, grad_shard=None, d_grad_params=None,
+                     master_shard, m_shard, v_shard, fp8_shard=None, d_fp8_params=None,
+                     scale_shard, b0: int, b1: int, d_sumsq, d_found_inf, stream=None):
+    """fp8z1_step reading grads folded or row-major, writing codes folded
+    and/or row-major."""
+    _check(lib().fp8z1_step_fused(layout.handle, C.byref(hp), _ptr(grad_shard), _ptr(d_grad_params),
+                                  _ptr(master_shard), _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard),
+                                  _ptr(d_fp8_params), _ptr(scale_shard), int(b0), int(b1),
+                                  _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_step_fused")
 
 
 def fp8z1_scaler_update(scaler: fp8z1_loss_scaler, found_inf: int):

@@ -7,6 +7,9 @@ follows on its shard [b0, b1):
   step : fold the (reduced) row-major grads of the shard, global grad norm
          ("DeepSpeed ZeRO 优化" §七), fused unscale + clip + AdamW + per-block
          E4M3 quantise, unfold the codes back into the row-major FP8 params;
+         with ``fused=True`` (the default) that is two kernels: the norm read
+         straight from the row-major grads, and the step reading the grads
+         through the block table and writing the codes row-major;
          the scales need no unfold: block order (e, rb, cb) makes the scale
          buffer of a param a [E, R/128, C/128] view.
   host : read found_inf and update the loss scale / step count (§六).
@@ -26,7 +29,7 @@ from . import fp8z1 as F
 class ShardOptimizer:
     def __init__(self, shapes: Sequence[Sequence[int]], *, dp_size: int = 1, rank: int = 0,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=1.0,
-                 loss_scale=1024.0, growth_interval=1000, device="cuda"):
+                 loss_scale=1024.0, growth_interval=1000, device="cuda", fused: bool = True):
         self.device = torch.device(device)
         self.layout = F.fp8z1_build_layout(shapes, dp_size)
         self.shapes = self.layout.shapes
@@ -38,7 +41,9 @@ class ShardOptimizer:
         self.master = torch.zeros(n, dtype=torch.float32, **kw)
         self.m = torch.zeros(n, dtype=torch.float32, **kw)
         self.v = torch.zeros(n, dtype=torch.float32, **kw)
-        self.grad = torch.zeros(n, dtype=torch.float32, **kw)
+        self.fused = fused
+        # the folded grads are only materialised on the unfused path
+        self.grad = None if fused else torch.zeros(n, dtype=torch.float32, **kw)
         self.codes = torch.zeros(n, dtype=torch.uint8, **kw)
         self.scales = torch.ones(nb, dtype=torch.float32, **kw)
         self.sumsq = torch.zeros(1, dtype=torch.float64, **kw)
@@ -116,13 +121,27 @@ class ShardOptimizer:
     def launch_step(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
                     stream=None):
         """Enqueue one step (no host synchronisation)."""
-        self.fold_into(grads, self.grad, stream)
         self.sumsq.zero_()
         self.found_inf.zero_()
+        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
+        if self.fused:
+            gptrs = self._ptrs(grads)
+            F.fp8z1_fold_norm(self.layout, gptrs, None, self.b0, self.b1, self.sumsq, self.found_inf,
+                              stream)
+            if self.norm_hook is not None:
+                self.norm_hook(self.sumsq, self.found_inf)
+            # codes go row-major when FP8 params are given, else to the folded buffer
+            F.fp8z1_step_fused(self.layout, hp, d_grad_params=gptrs, master_shard=self.master,
+                               m_shard=self.m, v_shard=self.v,
+                               fp8_shard=self.codes if fp8_params is None else None,
+                               d_fp8_params=None if fp8_params is None else self._ptrs(fp8_params),
+                               scale_shard=self.scales, b0=self.b0, b1=self.b1, d_sumsq=self.sumsq,
+                               d_found_inf=self.found_inf, stream=stream)
+            return
+        self.fold_into(grads, self.grad, stream)
         F.fp8z1_grad_norm(self.layout, self.grad, self.b0, self.b1, self.sumsq, self.found_inf, stream)
         if self.norm_hook is not None:
             self.norm_hook(self.sumsq, self.found_inf)
-        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
         F.fp8z1_step(self.layout, hp, self.grad, self.master, self.m, self.v, self.codes, self.scales,
                      self.b0, self.b1, self.sumsq, self.found_inf, stream)
         if fp8_params is not None:

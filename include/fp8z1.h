@@ -222,6 +222,43 @@ int fp8z1_step(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float
                float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
                const int32_t* d_found_inf, void* stream);
 
+/* ---- fused forms: the same results in fewer HBM passes --------------------- */
+
+/* Fold of the FP32 grads fused with the grad norm (§参数布局变换, §总结;
+ * "DeepSpeed ZeRO 优化" §七): reads the real grads of blocks [b0, b1) from the
+ * row-major params, adds their sum of squares to *d_sumsq and ORs inf/nan into
+ * *d_found_inf -- as fp8z1_grad_norm does on the folded range -- and, when
+ * `grad_shard` is not NULL, also stores the folded blocks there (as
+ * fp8z1_fold with elem_size 4).  With grad_shard NULL nothing is folded: the
+ * norm is taken straight from the row-major grads, for fp8z1_step_fused to
+ * read them the same way.  `d_grad_params`: DEVICE array of n_params DEVICE
+ * pointers to FP32 row-major params (4-byte aligned).  A null or misaligned
+ * entry sets FP8Z1_DEVSTATUS_BADPTR and *d_found_inf (so the step is skipped).
+ * The same reduction as fp8z1_grad_norm: deterministic for a given device and
+ * range, within about 1e-13 of the exact sum; it uses the same layout
+ * workspace, so calls sharing a layout must not overlap on the device.
+ * Errors: EINVAL, EALIGN, ENODEV, ECUDA. */
+int fp8z1_fold_norm(const fp8z1_layout* layout, const float* const* d_grad_params, float* grad_shard,
+                    int64_t b0, int64_t b1, double* d_sumsq, int32_t* d_found_inf, void* stream);
+
+/* fp8z1_step with the grad fold and the code unfold fused in (§总结: fold
+ * grads ... update ... quantise ... unfold params).  Grads come from exactly
+ * one of `grad_shard` (folded, as fp8z1_step) or `d_grad_params` (DEVICE
+ * array of DEVICE pointers to the row-major FP32 grads, read through the
+ * block lookup table).  Codes go to `fp8_shard` (folded, 16-byte aligned)
+ * and/or `d_fp8_params` (DEVICE array of DEVICE pointers to the row-major
+ * uint8 FP8 params, written on their real elements only: the fused unfold).
+ * Master / m / v / scales and every numerical result are those of
+ * fp8z1_step.  A null grad or FP8 param pointer (or a grad pointer that is not
+ * 4-byte aligned) leaves that block untouched and sets
+ * FP8Z1_DEVSTATUS_BADPTR.  Errors: EINVAL (both or neither grad source, no
+ * code destination, ...), EALIGN, ENODEV, ECUDA. */
+int fp8z1_step_fused(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                     const float* const* d_grad_params, float* master_shard, float* m_shard,
+                     float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
+                     float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
+                     const int32_t* d_found_inf, void* stream);
+
 /* ---- loss scaling (host; "DeepSpeed ZeRO 优化" §六, §九 Q6) ---------------- */
 
 /* After a step whose found_inf flag the host has read: found_inf != 0 halves
