@@ -101,6 +101,14 @@ def lib():
             L.oracle_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
             L.oracle_step.restype = C.c_int
             L.oracle_scaler_update.argtypes = [C.POINTER(ScalerState), i32]
+            L.oracle_paramwise_split.argtypes = [C.POINTER(Shape), i32, i32, P, P]
+            L.oracle_quant_monitor.argtypes = [P, P, C.c_float, i64, C.POINTER(C.c_double),
+                                               C.POINTER(i64)]
+            L.oracle_e8m0_decode.argtypes = [C.c_uint8]
+            L.oracle_e8m0_decode.restype = C.c_float
+            L.oracle_mx_quantise_group.argtypes = [P, P, P]
+            L.oracle_mx_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
+            L.oracle_mx_step.restype = C.c_int
             _lib = L
     return _lib
 
@@ -307,3 +315,59 @@ class Scaler:
     @property
     def good_steps(self):
         return self.s.good_steps
+
+
+# ---------------------------------------------------------------------------
+# param-wise split, quantisation monitors, MXFP8
+
+def paramwise_split(shapes, dp: int):
+    """(owner[n], bucket_elems[dp]) of the greedy param-wise split."""
+    arr, n = _shapes(shapes)
+    owner = np.zeros(max(1, n), np.int32)
+    bucket = np.zeros(max(1, dp), np.int64)
+    lib().oracle_paramwise_split(arr, n, int(dp), owner.ctypes.data, bucket.ctypes.data)
+    return owner[:n], bucket[:dp]
+
+
+def quant_monitor(p: np.ndarray, q: np.ndarray, scale: float):
+    """(cosine, underflow count) of one block."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    assert p.size == q.size
+    c, u = C.c_double(), C.c_int64()
+    lib().oracle_quant_monitor(p.ctypes.data, q.ctypes.data, float(scale), p.size, C.byref(c), C.byref(u))
+    return c.value, u.value
+
+
+MX_GROUP = 32
+
+
+def e8m0_decode(e: int) -> float:
+    return float(lib().oracle_e8m0_decode(int(e)))
+
+
+def mx_quantise(p: np.ndarray):
+    """Codes and E8M0 scale codes of consecutive groups of 32 values."""
+    p = np.ascontiguousarray(p, dtype=np.float32).reshape(-1)
+    assert p.size % MX_GROUP == 0
+    q = np.empty(p.size, np.uint8)
+    sc = np.empty(p.size // MX_GROUP, np.uint8)
+    for g in range(sc.size):
+        lib().oracle_mx_quantise_group(p[g * 32:].ctypes.data, q[g * 32:].ctypes.data,
+                                       sc[g:].ctypes.data)
+    return q, sc
+
+
+def mx_step(hp: HP, sumsq_value: float, found_inf: int, grad, master, m, v):
+    """AdamW + MXFP8 quantise over flat groups of 32; master/m/v in place.
+    Returns (codes uint8[n], E8M0 scale codes uint8[n/32], skipped)."""
+    n = grad.size
+    assert n % MX_GROUP == 0
+    for a in (grad, master, m, v):
+        assert a.dtype == np.float32 and a.size == n and a.flags["C_CONTIGUOUS"]
+    codes = np.zeros(n, np.uint8)
+    scales = np.zeros(n // MX_GROUP, np.uint8)
+    skipped = lib().oracle_mx_step(C.byref(hp), float(sumsq_value), int(found_inf), grad.ctypes.data,
+                                   master.ctypes.data, m.ctypes.data, v.ctypes.data,
+                                   codes.ctypes.data, scales.ctypes.data, n // MX_GROUP)
+    return codes, scales, bool(skipped)

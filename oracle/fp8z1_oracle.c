@@ -489,3 +489,136 @@ void oracle_e4m3_decode_n(const uint8_t* q, float* x, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) x[i] = oracle_e4m3_decode(q[i]);
 }
+
+/* ========================================================================= */
+/* Param-wise split [ZF §参数粒度切分]                                        */
+/* ========================================================================= */
+
+/* The page's alternative to the block-wise split: sort the FP8 params by size
+ * (largest first; equal sizes keep their given order), hand each in turn to
+ * the DP bucket holding the fewest elements so far (the lowest bucket index on
+ * a tie), then pad every bucket up to the largest one.  Size = E * R * C real
+ * elements.  owner[i] = bucket of param i; bucket[b] = elements in bucket b
+ * before padding. */
+void oracle_paramwise_split(const orc_shape* shapes, int32_t n, int32_t dp, int32_t* owner,
+                            int64_t* bucket)
+{
+    int32_t* order = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n ? n : 1));
+    for (int32_t i = 0; i < n; ++i) order[i] = i;
+    /* insertion sort: larger first, ties in index order (stable) */
+    for (int32_t i = 1; i < n; ++i) {
+        int32_t cur = order[i];
+        int64_t sz = shapes[cur].E * shapes[cur].R * shapes[cur].C;
+        int32_t j = i - 1;
+        while (j >= 0) {
+            int32_t o = order[j];
+            int64_t so = shapes[o].E * shapes[o].R * shapes[o].C;
+            if (so >= sz) break;
+            order[j + 1] = o;
+            --j;
+        }
+        order[j + 1] = cur;
+    }
+    for (int32_t b = 0; b < dp; ++b) bucket[b] = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        int32_t i = order[t];
+        int32_t best = 0;
+        for (int32_t b = 1; b < dp; ++b)
+            if (bucket[b] < bucket[best]) best = b;
+        owner[i] = best;
+        bucket[best] += shapes[i].E * shapes[i].R * shapes[i].C;
+    }
+    free(order);
+}
+
+/* ========================================================================= */
+/* Quantisation-error monitors ["FP8训练技术与万亿参数模型优化实践" §1.2]         */
+/* ========================================================================= */
+
+/* The page watches two numbers: Underflow = zeros / total (healthy below 0.5%)
+ * and Distortion = cosine(original, dequantised) (healthy above 0.995).
+ * Reading, per block of n values: underflow = the count of non-zero master
+ * values whose code decodes to 0 (the host divides by the block's real
+ * elements); cosine = sum(p d) / sqrt(sum(p^2) sum(d^2)) with
+ * d = decode(q) * scale, in double; 1 when both vectors are 0, 0 when only one
+ * is. */
+void oracle_quant_monitor(const float* p, const uint8_t* q, float scale, int64_t n, double* cosine,
+                          int64_t* underflow)
+{
+    double pd = 0.0, pp = 0.0, dd = 0.0;
+    int64_t under = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        double dq = (double)oracle_e4m3_decode(q[i]);
+        double d = dq * (double)scale;
+        double x = (double)p[i];
+        pd += x * d;
+        pp += x * x;
+        dd += d * d;
+        if (p[i] != 0.0f && dq == 0.0) ++under;
+    }
+    if (pp == 0.0 && dd == 0.0)
+        *cosine = 1.0;
+    else if (pp == 0.0 || dd == 0.0)
+        *cosine = 0.0;
+    else
+        *cosine = pd / sqrt(pp * dd);
+    *underflow = under;
+}
+
+/* ========================================================================= */
+/* MXFP8 [ZF §Blockwise 量化: MXFP8 gives each memory-contiguous block an      */
+/* E8M0 scale]; format per the OCP Microscaling (MX) specification v1.0       */
+/* ========================================================================= */
+
+#define ORC_MX_GROUP 32
+
+/* E8M0: an unsigned exponent, value 2^(e - 127) for e in [0, 254]; 255 is NaN. */
+float oracle_e8m0_decode(uint8_t e)
+{
+    if (e == 255) return NAN;
+    return ldexpf(1.0f, (int)e - 127);
+}
+
+/* One group of 32 consecutive values: the shared scale is
+ * X = 2^(floor(log2(amax)) - 8) (8 = the exponent of E4M3's largest normal,
+ * 448 = 1.75 * 2^8), clamped to the E8M0 range 2^-127 .. 2^127; each element is
+ * E4M3(p / X), rounded to nearest even, with values past 448 saturated.
+ * Reading where the specification leaves a choice: a group whose amax is 0
+ * gets X = 1 (code 127), as the block-wise scheme uses scale 1 there. */
+void oracle_mx_quantise_group(const float* p, uint8_t* q, uint8_t* scale_code)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < ORC_MX_GROUP; ++i) {
+        float a = fabsf(p[i]);
+        if (a > amax) amax = a;
+    }
+    int s = 0;
+    if (amax > 0.0f) {
+        int k = 0;
+        (void)frexpf(amax, &k); /* amax = f * 2^k, f in [0.5, 1): floor(log2) = k - 1 */
+        s = (k - 1) - 8;
+        if (s < -127) s = -127;
+        if (s > 127) s = 127;
+    }
+    *scale_code = (uint8_t)(s + 127);
+    float x = ldexpf(1.0f, s);
+    for (int i = 0; i < ORC_MX_GROUP; ++i) q[i] = oracle_e4m3_encode(p[i] / x);
+}
+
+/* The optimizer step on n_groups consecutive groups of 32 values of a flat
+ * row-major shard: the same unscale + clip + AdamW as oracle_step, then the
+ * MXFP8 quantiser per group.  Returns 1 (and writes nothing) when found_inf. */
+int oracle_mx_step(const orc_hp* hp, double sumsq, int32_t found_inf, const float* grad,
+                   float* master, float* m, float* v, uint8_t* codes, uint8_t* scales,
+                   int64_t n_groups)
+{
+    if (found_inf) return 1;
+    orc_derived d = derive(hp, sumsq);
+    for (int64_t g = 0; g < n_groups; ++g) {
+        int64_t base = g * ORC_MX_GROUP;
+        for (int64_t i = 0; i < ORC_MX_GROUP; ++i)
+            adamw_element(hp, &d, grad[base + i], &master[base + i], &m[base + i], &v[base + i]);
+        oracle_mx_quantise_group(master + base, codes + base, &scales[g]);
+    }
+    return 0;
+}
