@@ -338,6 +338,102 @@ def bench_ours(args, rank, world, dist):
     return out
 
 
+def bench_mx(args, rank, world, dist):
+    """The MXFP8 variant on the same workload: flat row-major state, a step is
+    the grad norm + the fused update with the MX quantiser (no fold, no table)."""
+    import torch
+
+    from blockwise_fp8_zero_fold_gb300 import build as fp8build
+    from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
+    from blockwise_fp8_zero_fold_gb300 import synth
+    from blockwise_fp8_zero_fold_gb300.optimizer import MxShardOptimizer
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fp8build.build()
+    if dist is not None:
+        dist.barrier()
+    F.lib()
+    w = synth.workload(args.workload, dp=1, rank=0)
+    if args.experts:
+        w = synth.workload(args.workload, dp=1, rank=0,
+                           shapes=[(min(e, args.experts), r, c) for e, r, c in w.shapes])
+    opt = MxShardOptimizer(w.shapes, device=dev, loss_scale=w.loss_scale,
+                           growth_interval=w.growth_interval,
+                           **{k: v for k, v in w.hp().items() if k != "loss_scale"})
+    n = opt.n_elems
+
+    def flat_into(dst, tensors):
+        off = 0
+        for t in tensors:
+            dst[off:off + t.numel()].copy_(t.reshape(-1))
+            off += t.numel()
+
+    for kind, buf in (("master", opt.master), ("m", opt.m), ("v", opt.v)):
+        flat_into(buf, synth.make_state(w, kind, dev))
+    grad = torch.empty(n, dtype=torch.float32, device=dev)
+    flat_into(grad, synth.make_grads(w, 1, dev))
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        opt.step(grad)
+    torch.cuda.synchronize()
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for k in ("norm", "step")}
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
+    t0.record(stream)
+    skipped = 0
+    for i in range(args.steps):
+        ev["norm"][i][0].record(stream)
+        opt.sumsq.zero_()
+        opt.found_inf.zero_()
+        F.fp8z1_mx_grad_norm(opt.layout, grad, opt.g0, opt.g1, opt.sumsq, opt.found_inf)
+        ev["norm"][i][1].record(stream)
+        hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
+        ev["step"][i][0].record(stream)
+        F.fp8z1_mx_step(opt.layout, hp, grad, opt.master, opt.m, opt.v, opt.codes, opt.scales,
+                        opt.g0, opt.g1, opt.sumsq, opt.found_inf)
+        ev["step"][i][1].record(stream)
+        skipped += opt.finish_step()
+    t1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    peak, peak_kind = _peak_hbm()
+    step_bytes = 29 * n + n // 32
+    achieved = step_bytes / (kern["step"] / 1e3) / 1e9
+    return {
+        "metric": METRIC,
+        "value": whole_job_rate(n, world, args.steps, elapsed_ms / 1e3),
+        "unit": "elem/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
+        "config": {"workload": f"{args.workload} in the MXFP8 layout (E8M0 scale per 32 elements): "
+                               + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
+                   "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)",
+                   "l2": "inputs larger than L2, no flush"},
+        "scheme": "mx", "gpu_launches": 2 * args.steps, "kernels_ms": kern,
+        "kernels_gbs": {"norm": 4 * n / kern["norm"] / 1e6, "step": achieved},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "fp8z1_mx_step",
+                     "peak_source": peak_kind, "bytes_per_launch": step_bytes},
+        "clocks": clk, "skipped_steps": skipped, "e2e": None,
+    }
+
+
 def _step_source_sha():
     import hashlib
     p = os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", "step.cu")
@@ -428,6 +524,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="moe")
+    ap.add_argument("--scheme", choices=["block", "mx"], default="block",
+                    help="block: 128x128 blockwise FP8 (the method); mx: the MXFP8 variant")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
                     help="fused: norm from row-major grads + step with fused fold/unfold (2 passes); "
                          "unfused: fold, norm, step, unfold (4 passes)")
@@ -455,7 +553,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         td.init_process_group("nccl")
         dist = td
-    out = bench_ours(args, rank, world, dist)
+    out = bench_mx(args, rank, world, dist) if args.scheme == "mx" else bench_ours(args, rank, world, dist)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:

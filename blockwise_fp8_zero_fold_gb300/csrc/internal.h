@@ -29,6 +29,20 @@ struct fp8z1_layout {
     int max_partials = 0;
 };
 
+// MXFP8 layout: the params' row-major elements back to back, cut into groups
+// of 32 consecutive elements (every C a multiple of 32).
+struct fp8z1_mx_layout {
+    std::vector<fp8z1_shape> shapes;
+    int32_t n_params = 0;
+    int32_t dp_size = 1;
+    int64_t n_groups = 0;
+    bool on_device = false;
+    int sm_count = 0;
+    double* d_partials = nullptr;  // grad-norm workspace: one double per CTA
+    unsigned* d_counter = nullptr;
+    int max_partials = 0;
+};
+
 namespace fp8z1 {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

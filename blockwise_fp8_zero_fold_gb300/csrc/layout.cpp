@@ -7,6 +7,7 @@
 // §参数布局变换: block order of fold is (expert, row block, col block).
 #include <limits.h>
 
+#include <algorithm>
 #include <new>
 
 #include "internal.h"
@@ -183,6 +184,128 @@ extern "C" int fp8z1_scaler_update(fp8z1_loss_scaler* s, int32_t found_inf)
         s->scale *= 2.0f;
         s->good_steps = 0;
     }
+    return FP8Z1_OK;
+}
+
+// "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §参数粒度切分: the page's other
+// split.  Params sorted by size, largest first (equal sizes keep their order),
+// each given to the DP bucket with the fewest elements so far (the lowest
+// index on a tie); every bucket is then padded to the largest.
+extern "C" int fp8z1_paramwise_split(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                                     int32_t* owner, int64_t* bucket_elems, int64_t* padded_total)
+{
+    if (!shapes || n_params < 1 || dp_size < 1 || !owner || !bucket_elems) return FP8Z1_EINVAL;
+    std::vector<int64_t> size((size_t)n_params);
+    for (int32_t i = 0; i < n_params; ++i) {
+        const fp8z1_shape s = shapes[i];
+        if (s.E < 1 || s.R < 1 || s.C < 1 || s.R > INT64_MAX / s.C || s.E > INT64_MAX / (s.R * s.C))
+            return FP8Z1_EINVAL;
+        size[(size_t)i] = s.E * s.R * s.C;
+    }
+    std::vector<int32_t> order((size_t)n_params);
+    for (int32_t i = 0; i < n_params; ++i) order[(size_t)i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int32_t a, int32_t b) { return size[(size_t)a] > size[(size_t)b]; });
+    for (int32_t b = 0; b < dp_size; ++b) bucket_elems[b] = 0;
+    for (int32_t i : order) {
+        int32_t best = 0;
+        for (int32_t b = 1; b < dp_size; ++b)
+            if (bucket_elems[b] < bucket_elems[best]) best = b;
+        owner[i] = best;
+        bucket_elems[best] += size[(size_t)i];
+    }
+    if (padded_total) {
+        int64_t mx = 0;
+        for (int32_t b = 0; b < dp_size; ++b) mx = bucket_elems[b] > mx ? bucket_elems[b] : mx;
+        *padded_total = mx * dp_size;
+    }
+    return FP8Z1_OK;
+}
+
+// ---- MXFP8 layout --------------------------------------------------------
+
+extern "C" int fp8z1_mx_build_layout(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                                     uint32_t flags, fp8z1_mx_layout** out)
+{
+    if (!out) return FP8Z1_EINVAL;
+    *out = nullptr;
+    if (!shapes || n_params < 1 || dp_size < 1 || (flags & ~FP8Z1_LAYOUT_HOST_ONLY)) return FP8Z1_EINVAL;
+    int64_t groups = 0;
+    const int64_t kMax = INT64_MAX / FP8Z1_MX_GROUP;
+    for (int32_t i = 0; i < n_params; ++i) {
+        const fp8z1_shape s = shapes[i];
+        if (s.E < 1 || s.R < 1 || s.C < 1 || s.C % FP8Z1_MX_GROUP != 0) return FP8Z1_EINVAL;
+        const int64_t per_row = s.C / FP8Z1_MX_GROUP;
+        if (s.R > kMax / per_row || s.E > kMax / (s.R * per_row)) return FP8Z1_EINVAL;
+        const int64_t g = s.E * s.R * per_row;
+        if (g > kMax - groups) return FP8Z1_EINVAL;
+        groups += g;
+    }
+    fp8z1_mx_layout* L = new (std::nothrow) fp8z1_mx_layout();
+    if (!L) return FP8Z1_ENOMEM;
+    try {
+        L->shapes.assign(shapes, shapes + n_params);
+    } catch (...) {
+        delete L;
+        return FP8Z1_ENOMEM;
+    }
+    L->n_params = n_params;
+    L->dp_size = dp_size;
+    L->n_groups = groups;
+    if (!(flags & FP8Z1_LAYOUT_HOST_ONLY)) {
+        int dev = 0;
+        int st = FP8Z1_OK;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&L->sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            st = FP8Z1_ECUDA;
+        if (st == FP8Z1_OK) {
+            L->max_partials = L->sm_count * 4 < 4096 ? L->sm_count * 4 : 4096;
+            if (cudaMalloc(&L->d_partials, sizeof(double) * (size_t)L->max_partials) != cudaSuccess ||
+                cudaMalloc(&L->d_counter, sizeof(unsigned)) != cudaSuccess)
+                st = FP8Z1_ENOMEM;
+            else if (cudaMemset(L->d_counter, 0, sizeof(unsigned)) != cudaSuccess ||
+                     cudaDeviceSynchronize() != cudaSuccess)
+                st = FP8Z1_ECUDA;
+        }
+        if (st != FP8Z1_OK) {
+            cudaGetLastError();
+            cudaFree(L->d_partials);
+            cudaFree(L->d_counter);
+            delete L;
+            return st;
+        }
+        L->on_device = true;
+    }
+    *out = L;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_mx_destroy_layout(fp8z1_mx_layout* L)
+{
+    if (!L) return FP8Z1_OK;
+    if (L->on_device) {
+        cudaFree(L->d_partials);
+        cudaFree(L->d_counter);
+    }
+    delete L;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_mx_layout_info(const fp8z1_mx_layout* L, int64_t* n_groups, int64_t* n_elems)
+{
+    if (!L) return FP8Z1_EINVAL;
+    if (n_groups) *n_groups = L->n_groups;
+    if (n_elems) *n_elems = L->n_groups * FP8Z1_MX_GROUP;
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_mx_shard_range(const fp8z1_mx_layout* L, int32_t rank, int64_t* g0, int64_t* g1)
+{
+    if (!L || !g0 || !g1 || rank < 0 || rank >= L->dp_size) return FP8Z1_EINVAL;
+    const int64_t per = (L->n_groups + L->dp_size - 1) / L->dp_size;
+    const int64_t lo = per * rank, hi = per * (rank + 1);
+    *g0 = lo < L->n_groups ? lo : L->n_groups;
+    *g1 = hi < L->n_groups ? hi : L->n_groups;
     return FP8Z1_OK;
 }
 

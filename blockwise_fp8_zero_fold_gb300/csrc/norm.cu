@@ -137,7 +137,9 @@ struct NormArgs {
     const float* const* params;   // ROWS: row-major FP32 grads
     float4* store;                // STORE: folded grads at block b0
     int64_t b0;                   // first block (ROWS: LUT index)
-    int64_t nblocks;
+    int64_t nblocks;              // blocks of 16384, the last one possibly partial
+    int64_t tail_k;               // !ROWS: index of a partial last block ...
+    int tail_vec4;                // ... and its float4 count (0: no partial block)
     double* partials;             // one per CTA
     unsigned* counter;
     unsigned* status;
@@ -152,29 +154,36 @@ template <bool ROWS>
 __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
                                            float4 (&x)[kVec])
 {
-    if (!ROWS) {
+    if constexpr (!ROWS) {
         const float4* p = a.g + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+        if (a.tail_vec4 != 0 && k == a.tail_k) {  // a flat range's partial last block
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                x[j] = tid + j * kThreads < a.tail_vec4 ? __ldcs(p + j * kThreads)
+                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-        const int ci = tid + j * kThreads;
-        const int r = ci >> 5, c = (ci & 31) << 2;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!s.bad && r < s.rows) {
-            const float* src = s.tile + r * s.ld + c;
-            if (s.vec) {  // a 4-column group is then all real or all padding
-                if (c < s.cols) v = __ldcs(reinterpret_cast<const float4*>(src));
-            } else {
-                if (c + 0 < s.cols) v.x = __ldcs(src + 0);
-                if (c + 1 < s.cols) v.y = __ldcs(src + 1);
-                if (c + 2 < s.cols) v.z = __ldcs(src + 2);
-                if (c + 3 < s.cols) v.w = __ldcs(src + 3);
+        for (int j = 0; j < kVec; ++j) {
+            const int ci = tid + j * kThreads;
+            const int r = ci >> 5, c = (ci & 31) << 2;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!s.bad && r < s.rows) {
+                const float* src = s.tile + r * s.ld + c;
+                if (s.vec) {  // a 4-column group is then all real or all padding
+                    if (c < s.cols) v = __ldcs(reinterpret_cast<const float4*>(src));
+                } else {
+                    if (c + 0 < s.cols) v.x = __ldcs(src + 0);
+                    if (c + 1 < s.cols) v.y = __ldcs(src + 1);
+                    if (c + 2 < s.cols) v.z = __ldcs(src + 2);
+                    if (c + 3 < s.cols) v.w = __ldcs(src + 3);
+                }
             }
+            x[j] = v;
         }
-        x[j] = v;
     }
 }
 
@@ -335,6 +344,36 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
         norm_kernel<true, true><<<grid, kThreads, 0, s>>>(a);
     else
         norm_kernel<true, false><<<grid, kThreads, 0, s>>>(a);
+    return fp8z1::launch_status();
+}
+
+// The grad norm of an MXFP8 shard: a flat range of (g1 - g0) groups of 32
+// FP32 grads, in the same reduction (its last 16384-element block may be
+// partial).
+extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_shard, int64_t g0,
+                                  int64_t g1, double* d_sumsq, int32_t* d_found_inf, void* stream)
+{
+    if (!L || !grad_shard || !d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
+    if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    const int64_t n = (g1 - g0) * FP8Z1_MX_GROUP;
+    if (n == 0) return FP8Z1_OK;
+    NormArgs a = {};
+    a.g = reinterpret_cast<const float4*>(grad_shard);
+    const int64_t full = n / FP8Z1_BLOCK_ELEMS, rem = n % FP8Z1_BLOCK_ELEMS;
+    a.nblocks = full + (rem ? 1 : 0);
+    a.tail_k = full;
+    a.tail_vec4 = (int)(rem / 4);
+    a.partials = L->d_partials;
+    a.counter = L->d_counter;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    int64_t grid = L->sm_count;
+    if (grid > a.nblocks) grid = a.nblocks;
+    if (grid > L->max_partials) grid = L->max_partials;
+    norm_kernel<false, false><<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
 

@@ -62,6 +62,8 @@ struct StepArgs {
     const float* const* grad_params;  // GRAD_ROWS: row-major FP32 grads
     uint8_t* const* code_params;      // CODES_ROWS: row-major FP8 params
     unsigned* status;
+    float* block_cos;            // MON: cosine(master, dequantised) per block
+    uint32_t* block_underflow;   // MON: non-zero masters whose code is 0, per block
     StepScalars c;
 };
 
@@ -82,6 +84,17 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
     unsigned short r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// two E4M3 codes (low byte -> .x) -> their exact values
+__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two)
+{
+    uint32_t h2;
+    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
+    float lo, hi;
+    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+    return make_float2(lo, hi);
 }
 
 __device__ __forceinline__ float warp_max(float v)
@@ -124,7 +137,23 @@ __device__ __forceinline__ void store_codes_rows(uint8_t* tile, int64_t ld, int 
     }
 }
 
-template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED>
+// Quantisation monitors ("FP8训练技术与万亿参数模型优化实践" §1.2: underflow =
+// zeros / total, distortion = cosine(original, dequantised)), per block: the
+// count of non-zero new masters whose code decodes to 0, and
+// sum(p d) / sqrt(sum(p^2) sum(d^2)) with d = decode(code) * scale (1 when both
+// are all zero, 0 when only one is).  FP32 sums per thread, double across the
+// CTA: a diagnostic, not bit-exact.
+__device__ __forceinline__ void monitor_add(float p, float dec, float scale, float& pd, float& pp,
+                                            float& dd, uint32_t& under)
+{
+    const float d = __fmul_rn(dec, scale);
+    pd = __fmaf_rn(p, d, pd);
+    pp = __fmaf_rn(p, p, pp);
+    dd = __fmaf_rn(d, d, dd);
+    under += (p != 0.0f && dec == 0.0f) ? 1u : 0u;
+}
+
+template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
@@ -214,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     const float scale = bmax == 0.0f ? 1.0f : __fdiv_rn(bmax, 448.0f);
     if (tid == 0) a.scales[blockIdx.x] = scale;
 
+    float pd = 0.0f, pp = 0.0f, dd = 0.0f;
+    uint32_t under = 0u;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         const uint32_t lo = e4m3x2(__fdiv_rn(pn[4 * j + 0], scale), __fdiv_rn(pn[4 * j + 1], scale));
@@ -223,6 +254,147 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         if (CODES_ROWS) {
             const int ci = tid + j * kThreads;
             store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
+        }
+        if (MON) {
+            const float2 d01 = e4m3x2_decode(lo), d23 = e4m3x2_decode(hi);
+            monitor_add(pn[4 * j + 0], d01.x, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 1], d01.y, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 2], d23.x, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 3], d23.y, scale, pd, pp, dd, under);
+        }
+    }
+    if (MON) {
+        __shared__ float s_mon[3][kWarps];
+        __shared__ uint32_t s_under[kWarps];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            pd += __shfl_xor_sync(0xffffffffu, pd, o);
+            pp += __shfl_xor_sync(0xffffffffu, pp, o);
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+            under += __shfl_xor_sync(0xffffffffu, under, o);
+        }
+        if ((tid & 31) == 0) {
+            s_mon[0][tid >> 5] = pd;
+            s_mon[1][tid >> 5] = pp;
+            s_mon[2][tid >> 5] = dd;
+            s_under[tid >> 5] = under;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            double tpd = 0.0, tpp = 0.0, tdd = 0.0;
+            uint32_t tu = 0u;
+            for (int w = 0; w < kWarps; ++w) {
+                tpd += s_mon[0][w];
+                tpp += s_mon[1][w];
+                tdd += s_mon[2][w];
+                tu += s_under[w];
+            }
+            float cosv;
+            if (tpp == 0.0 && tdd == 0.0)
+                cosv = 1.0f;
+            else if (tpp == 0.0 || tdd == 0.0)
+                cosv = 0.0f;
+            else
+                cosv = (float)(tpd / sqrt(tpp * tdd));
+            a.block_cos[blockIdx.x] = cosv;
+            a.block_underflow[blockIdx.x] = tu;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §Blockwise 量化: the
+// Blackwell format that gives every memory-contiguous block its own E8M0
+// scale; OCP MX specification v1.0).  The shard is a flat run of the params'
+// row-major elements; a group of 32 consecutive values shares the scale
+// X = 2^(floor(log2 amax) - 8), clamped to 2^-127 .. 2^127 (X = 1 when
+// amax = 0), stored as the E8M0 code log2(X) + 127, and each value becomes
+// E4M3(p / X), rounded to nearest even and saturated at 448.  Because the
+// groups are contiguous there is no fold, no table and no block barrier: a
+// group is 8 consecutive lanes (one float4 each), its amax three shuffles.
+constexpr int kMxThreads = 256;
+
+struct MxArgs {
+    const float4* grad;
+    float4* master;
+    float4* mom1;
+    float4* mom2;
+    uint32_t* codes;
+    uint8_t* scales;   // one E8M0 code per group
+    const double* sumsq;
+    const int32_t* found_inf;
+    int64_t n_chunks;  // float4 chunks: 8 per group
+    StepScalars c;
+};
+
+// Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
+// u, its 32 lanes hold 4 whole groups) and issues every load of them before
+// any update, so four chunks' loads are in flight per thread.
+constexpr int kMxUnroll = 4;
+
+__global__ void __launch_bounds__(kMxThreads) mx_step_kernel(const MxArgs a)
+{
+    if (*a.found_inf != 0) return;  // skipped step: write nothing
+    __shared__ float s_gscale;
+    if (threadIdx.x == 0) {
+        const double global = sqrt(*a.sumsq) / (double)a.c.loss_scale;
+        const double coef = (double)a.c.max_norm / (global + 1e-6);
+        const float clip = coef < 1.0 ? (float)coef : 1.0f;
+        s_gscale = __fdiv_rn(clip, a.c.loss_scale);
+    }
+    __syncthreads();
+    const float gs = s_gscale;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kMxThreads / 32);
+    // the trip count is uniform across a warp, so the group shuffles always see
+    // all 32 lanes; a group's 8 lanes are in or out of range together
+    for (int64_t wbase = warp * (32 * kMxUnroll); wbase < a.n_chunks; wbase += nwarps * (32 * kMxUnroll)) {
+        float4 g4[kMxUnroll], p4[kMxUnroll], m4[kMxUnroll], v4[kMxUnroll];
+#pragma unroll
+        for (int u = 0; u < kMxUnroll; ++u) {
+            const int64_t i = wbase + u * 32 + lane;
+            if (i < a.n_chunks) {
+                g4[u] = __ldcs(a.grad + i);
+                p4[u] = a.master[i];
+                m4[u] = a.mom1[i];
+                v4[u] = a.mom2[i];
+            } else {
+                g4[u] = p4[u] = m4[u] = v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMxUnroll; ++u) {
+            const int64_t i = wbase + u * 32 + lane;
+            const bool valid = i < a.n_chunks;
+            if (valid) {
+                adamw(gs, a.c, g4[u].x, p4[u].x, m4[u].x, v4[u].x);
+                adamw(gs, a.c, g4[u].y, p4[u].y, m4[u].y, v4[u].y);
+                adamw(gs, a.c, g4[u].z, p4[u].z, m4[u].z, v4[u].z);
+                adamw(gs, a.c, g4[u].w, p4[u].w, m4[u].w, v4[u].w);
+                __stcs(a.mom1 + i, m4[u]);
+                __stcs(a.mom2 + i, v4[u]);
+                __stcs(a.master + i, p4[u]);
+            }
+            const float4 p = p4[u];
+            float amax = fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w)));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            // floor(log2 amax) - 8 from the exponent field (a subnormal amax has
+            // field 0 and clamps to -127); 2^-s is then a normal float
+            int sexp = 0;
+            if (amax != 0.0f) {
+                sexp = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 8;
+                sexp = sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
+            }
+            const float inv = __uint_as_float((uint32_t)(127 - sexp) << 23);
+            const uint32_t lo = e4m3x2(__fmul_rn(p.x, inv), __fmul_rn(p.y, inv));
+            const uint32_t hi = e4m3x2(__fmul_rn(p.z, inv), __fmul_rn(p.w, inv));
+            if (valid) {
+                __stcs(a.codes + i, lo | (hi << 16));
+                if ((lane & 7) == 0) a.scales[i >> 3] = (uint8_t)(sexp + 127);
+            }
         }
     }
 }
@@ -270,10 +442,19 @@ int check_common(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* m
     return FP8Z1_OK;
 }
 
-template <bool GR, bool CR, bool CF>
+template <bool GR, bool CR, bool CF, bool MON>
 void launch(const StepArgs& a, int64_t nb, cudaStream_t s)
 {
-    step_kernel<GR, CR, CF><<<(unsigned)nb, kThreads, 0, s>>>(a);
+    step_kernel<GR, CR, CF, MON><<<(unsigned)nb, kThreads, 0, s>>>(a);
+}
+
+template <bool GR, bool CR, bool CF>
+void launch_mon(const StepArgs& a, int64_t nb, cudaStream_t s, bool mon)
+{
+    if (mon)
+        launch<GR, CR, CF, true>(a, nb, s);
+    else
+        launch<GR, CR, CF, false>(a, nb, s);
 }
 
 }  // namespace
@@ -301,14 +482,15 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
     a.b0 = b0;
     a.status = L->d_status;
     a.c = scalars(hp);
-    launch<false, false, true>(a, b1 - b0, static_cast<cudaStream_t>(stream));
+    launch<false, false, true, false>(a, b1 - b0, static_cast<cudaStream_t>(stream));
     return fp8z1::launch_status();
 }
 
 extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
                                 const float* const* d_grad_params, float* master_shard, float* m_shard,
                                 float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
-                                float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
+                                float* scale_shard, float* block_cos, uint32_t* block_underflow,
+                                int64_t b0, int64_t b1, const double* d_sumsq,
                                 const int32_t* d_found_inf, void* stream)
 {
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
@@ -316,6 +498,9 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
     // exactly one grad source, at least one code destination
     if ((grad_shard == nullptr) == (d_grad_params == nullptr)) return FP8Z1_EINVAL;
     if (fp8_shard == nullptr && d_fp8_params == nullptr) return FP8Z1_EINVAL;
+    if ((block_cos == nullptr) != (block_underflow == nullptr)) return FP8Z1_EINVAL;
+    if ((block_cos && !fp8z1::aligned(block_cos, 4)) || (block_underflow && !fp8z1::aligned(block_underflow, 4)))
+        return FP8Z1_EALIGN;
     if ((grad_shard && !fp8z1::aligned(grad_shard, 16)) || (fp8_shard && !fp8z1::aligned(fp8_shard, 16)) ||
         (d_grad_params && !fp8z1::aligned(d_grad_params, sizeof(void*))) ||
         (d_fp8_params && !fp8z1::aligned(d_fp8_params, sizeof(void*))))
@@ -334,19 +519,57 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
     a.b0 = b0;
     a.grad_params = d_grad_params;
     a.code_params = d_fp8_params;
+    a.block_cos = block_cos;
+    a.block_underflow = block_underflow;
     a.status = L->d_status;
     a.c = scalars(hp);
     const int64_t nb = b1 - b0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool gr = d_grad_params != nullptr, cr = d_fp8_params != nullptr, cf = fp8_shard != nullptr;
+    const bool mon = block_cos != nullptr;
     if (gr) {
-        if (cr && cf) launch<true, true, true>(a, nb, s);
-        else if (cr) launch<true, true, false>(a, nb, s);
-        else launch<true, false, true>(a, nb, s);
+        if (cr && cf) launch_mon<true, true, true>(a, nb, s, mon);
+        else if (cr) launch_mon<true, true, false>(a, nb, s, mon);
+        else launch_mon<true, false, true>(a, nb, s, mon);
     } else {
-        if (cr && cf) launch<false, true, true>(a, nb, s);
-        else if (cr) launch<false, true, false>(a, nb, s);
-        else launch<false, false, true>(a, nb, s);
+        if (cr && cf) launch_mon<false, true, true>(a, nb, s, mon);
+        else if (cr) launch_mon<false, true, false>(a, nb, s, mon);
+        else launch_mon<false, false, true>(a, nb, s, mon);
     }
+    return fp8z1::launch_status();
+}
+
+extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                             float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                             uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
+                             const int32_t* d_found_inf, void* stream)
+{
+    if (!L || !hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
+        !d_sumsq || !d_found_inf || !in_domain(hp))
+        return FP8Z1_EINVAL;
+    if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(master_shard, 16) || !fp8z1::aligned(m_shard, 16) ||
+        !fp8z1::aligned(v_shard, 16) || !fp8z1::aligned(fp8_shard, 16) || !fp8z1::aligned(d_sumsq, 8) ||
+        !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    const int64_t chunks = (g1 - g0) * (FP8Z1_MX_GROUP / 4);
+    if (chunks == 0) return FP8Z1_OK;
+    MxArgs a = {};
+    a.grad = reinterpret_cast<const float4*>(grad_shard);
+    a.master = reinterpret_cast<float4*>(master_shard);
+    a.mom1 = reinterpret_cast<float4*>(m_shard);
+    a.mom2 = reinterpret_cast<float4*>(v_shard);
+    a.codes = reinterpret_cast<uint32_t*>(fp8_shard);
+    a.scales = scale_shard;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    a.n_chunks = chunks;
+    a.c = scalars(hp);
+    // a persistent grid: 4 CTAs of 256 threads per SM, no more than the chunks need
+    int64_t grid = (int64_t)L->sm_count * 4;
+    const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
+    if (grid > need) grid = need;
+    mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }

@@ -21,6 +21,7 @@ _lock = threading.Lock()
 _lib = None
 
 BLOCK_ELEMS = 16384
+MX_GROUP = 32
 TILE = 128
 LAYOUT_HOST_ONLY = 1
 DEVSTATUS_BADPTR = 1
@@ -79,7 +80,17 @@ _SIGS = {
                              C.c_int64, _P, _P, _P]),
     "fp8z1_fold_norm": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_step_fused": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, _P, _P,
-                                   C.c_int64, C.c_int64, _P, _P, _P]),
+                                   _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_paramwise_split": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, _P, _P,
+                                        C.POINTER(C.c_int64)]),
+    "fp8z1_mx_build_layout": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, C.c_uint32,
+                                        C.POINTER(_P)]),
+    "fp8z1_mx_destroy_layout": (C.c_int, [_P]),
+    "fp8z1_mx_layout_info": (C.c_int, [_P, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "fp8z1_mx_shard_range": (C.c_int, [_P, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
+    "fp8z1_mx_grad_norm": (C.c_int, [_P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_mx_step": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, C.c_int64,
+                                C.c_int64, _P, _P, _P]),
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
@@ -258,14 +269,77 @@ def fp8z1_fold_norm(layout: Layout, d_grad_params, grad_shard, b0: int, b1: int,
 
 def fp8z1_step_fused(layout: Layout, hp: fp8z1_adamw_hp, *, grad_shard=None, d_grad_params=None,
                      master_shard, m_shard, v_shard, fp8_shard=None, d_fp8_params=None,
-                     scale_shard, b0: int, b1: int, d_sumsq, d_found_inf, stream=None):
+                     scale_shard, block_cos=None, block_underflow=None, b0: int, b1: int, d_sumsq,
+                     d_found_inf, stream=None):
     """fp8z1_step reading grads folded or row-major, writing codes folded
-    and/or row-major."""
+    and/or row-major, optionally with the per-block quantisation monitors."""
     _check(lib().fp8z1_step_fused(layout.handle, C.byref(hp), _ptr(grad_shard), _ptr(d_grad_params),
                                   _ptr(master_shard), _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard),
-                                  _ptr(d_fp8_params), _ptr(scale_shard), int(b0), int(b1),
+                                  _ptr(d_fp8_params), _ptr(scale_shard), _ptr(block_cos),
+                                  _ptr(block_underflow), int(b0), int(b1),
                                   _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_step_fused")
+
+
+def fp8z1_paramwise_split(shapes, dp_size: int):
+    """(owner[n], bucket_elems[dp], padded_total) of the greedy param-wise split."""
+    shapes = [_norm_shape(s) for s in shapes]
+    arr = (fp8z1_shape * max(1, len(shapes)))(*[fp8z1_shape(*s) for s in shapes])
+    owner = np.zeros(max(1, len(shapes)), np.int32)
+    bucket = np.zeros(max(1, dp_size), np.int64)
+    padded = C.c_int64()
+    _check(lib().fp8z1_paramwise_split(arr, len(shapes), int(dp_size), owner.ctypes.data,
+                                       bucket.ctypes.data, C.byref(padded)), "fp8z1_paramwise_split")
+    return owner[:len(shapes)], bucket[:dp_size], padded.value
+
+
+class MxLayout(Layout):
+    """Owner of an ``fp8z1_mx_layout*``."""
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            try:
+                lib().fp8z1_mx_destroy_layout(self.handle)
+            except Exception:
+                pass
+            self.handle = None
+
+
+def fp8z1_mx_build_layout(shapes, dp_size: int = 1, host_only: bool = False) -> MxLayout:
+    shapes = [_norm_shape(s) for s in shapes]
+    arr = (fp8z1_shape * max(1, len(shapes)))(*[fp8z1_shape(*s) for s in shapes])
+    out = _P()
+    _check(lib().fp8z1_mx_build_layout(arr, len(shapes), int(dp_size),
+                                       LAYOUT_HOST_ONLY if host_only else 0, C.byref(out)),
+           "fp8z1_mx_build_layout")
+    return MxLayout(out.value, shapes)
+
+
+def fp8z1_mx_layout_info(layout: MxLayout):
+    a, b = C.c_int64(), C.c_int64()
+    _check(lib().fp8z1_mx_layout_info(layout.handle, C.byref(a), C.byref(b)), "fp8z1_mx_layout_info")
+    return a.value, b.value
+
+
+def fp8z1_mx_shard_range(layout: MxLayout, rank: int):
+    a, b = C.c_int64(), C.c_int64()
+    _check(lib().fp8z1_mx_shard_range(layout.handle, int(rank), C.byref(a), C.byref(b)),
+           "fp8z1_mx_shard_range")
+    return a.value, b.value
+
+
+def fp8z1_mx_grad_norm(layout: MxLayout, grad_shard, g0: int, g1: int, d_sumsq, d_found_inf,
+                       stream=None):
+    _check(lib().fp8z1_mx_grad_norm(layout.handle, _ptr(grad_shard), int(g0), int(g1), _ptr(d_sumsq),
+                                    _ptr(d_found_inf), _stream(stream)), "fp8z1_mx_grad_norm")
+
+
+def fp8z1_mx_step(layout: MxLayout, hp: fp8z1_adamw_hp, grad_shard, master_shard, m_shard, v_shard,
+                  fp8_shard, scale_shard, g0: int, g1: int, d_sumsq, d_found_inf, stream=None):
+    _check(lib().fp8z1_mx_step(layout.handle, C.byref(hp), _ptr(grad_shard), _ptr(master_shard),
+                               _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard), _ptr(scale_shard),
+                               int(g0), int(g1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_mx_step")
 
 
 def fp8z1_scaler_update(scaler: fp8z1_loss_scaler, found_inf: int):

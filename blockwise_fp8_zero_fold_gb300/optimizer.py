@@ -156,3 +156,61 @@ class ShardOptimizer:
     def step(self, grads, fp8_params=None, stream=None) -> int:
         self.launch_step(grads, fp8_params, stream)
         return self.finish_step()
+
+
+class MxShardOptimizer:
+    """The same optimizer step with MXFP8 weights (E8M0 scale per 32
+    consecutive elements) instead of 128x128 blocks.
+
+    The blocks of MXFP8 are memory-contiguous ("面向 Blockwise FP8 量化的 ZeRO
+    优化器设计" §Blockwise 量化 / §Blockwise 量化给 ZeRO-1 带来的挑战), so no
+    fold or table is needed: the state is the params' row-major elements back
+    to back, the shard a flat run of whole groups, and a step is two kernels
+    (the grad norm, then the fused update + MX quantise).  Every C must be a
+    multiple of 32."""
+
+    def __init__(self, shapes: Sequence[Sequence[int]], *, dp_size: int = 1, rank: int = 0,
+                 lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=1.0,
+                 loss_scale=1024.0, growth_interval=1000, device="cuda"):
+        self.device = torch.device(device)
+        self.layout = F.fp8z1_mx_build_layout(shapes, dp_size)
+        self.shapes = self.layout.shapes
+        self.g0, self.g1 = F.fp8z1_mx_shard_range(self.layout, rank)
+        self.n_groups, self.n_elems = F.fp8z1_mx_layout_info(self.layout)
+        n = (self.g1 - self.g0) * F.MX_GROUP
+        kw = dict(device=self.device)
+        self.master = torch.zeros(n, dtype=torch.float32, **kw)
+        self.m = torch.zeros(n, dtype=torch.float32, **kw)
+        self.v = torch.zeros(n, dtype=torch.float32, **kw)
+        self.codes = torch.zeros(n, dtype=torch.uint8, **kw)
+        self.scales = torch.full((self.g1 - self.g0,), 127, dtype=torch.uint8, **kw)
+        self.sumsq = torch.zeros(1, dtype=torch.float64, **kw)
+        self.found_inf = torch.zeros(1, dtype=torch.int32, **kw)
+        self.hp = dict(lr=lr, beta1=beta1, beta2=beta2, eps=eps, weight_decay=weight_decay,
+                       max_norm=max_norm)
+        self.scaler = F.fp8z1_loss_scaler(float(loss_scale), 0, 0, int(growth_interval))
+        self.norm_hook: Optional[Callable[[torch.Tensor, torch.Tensor], None]] = None
+
+    def shard_of(self, flat: torch.Tensor) -> torch.Tensor:
+        """This rank's slice of a whole flat buffer (grads, say)."""
+        return flat[self.g0 * F.MX_GROUP:self.g1 * F.MX_GROUP]
+
+    def launch_step(self, grad_shard: torch.Tensor, stream=None):
+        self.sumsq.zero_()
+        self.found_inf.zero_()
+        F.fp8z1_mx_grad_norm(self.layout, grad_shard, self.g0, self.g1, self.sumsq, self.found_inf,
+                             stream)
+        if self.norm_hook is not None:
+            self.norm_hook(self.sumsq, self.found_inf)
+        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
+        F.fp8z1_mx_step(self.layout, hp, grad_shard, self.master, self.m, self.v, self.codes,
+                        self.scales, self.g0, self.g1, self.sumsq, self.found_inf, stream)
+
+    def finish_step(self) -> int:
+        found = int(self.found_inf.item())
+        F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
+    def step(self, grad_shard: torch.Tensor, stream=None) -> int:
+        self.launch_step(grad_shard, stream)
+        return self.finish_step()

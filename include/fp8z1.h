@@ -46,6 +46,7 @@ extern "C" {
 
 #define FP8Z1_TILE 128
 #define FP8Z1_BLOCK_ELEMS 16384
+#define FP8Z1_MX_GROUP 32
 
 /* status codes */
 #define FP8Z1_OK 0
@@ -251,13 +252,71 @@ int fp8z1_fold_norm(const fp8z1_layout* layout, const float* const* d_grad_param
  * Master / m / v / scales and every numerical result are those of
  * fp8z1_step.  A null grad or FP8 param pointer (or a grad pointer that is not
  * 4-byte aligned) leaves that block untouched and sets
- * FP8Z1_DEVSTATUS_BADPTR.  Errors: EINVAL (both or neither grad source, no
- * code destination, ...), EALIGN, ENODEV, ECUDA. */
+ * FP8Z1_DEVSTATUS_BADPTR.
+ * Quantisation monitors ("FP8训练技术与万亿参数模型优化实践" §1.2: underflow =
+ * zeros / total, healthy below 0.5%; distortion = cosine(original,
+ * dequantised), healthy above 0.995): when `block_cos` and
+ * `block_underflow` (device, b1 - b0 entries each, both or neither) are given,
+ * the kernel also writes per block the cosine between the new FP32 master
+ * and its dequantised FP8 value (decode(code) * scale; 1 when both are all
+ * zero) and the count of non-zero masters whose code decodes to 0 -- divide
+ * by the block's real elements (rows_real * cols_real of the LUT) for the
+ * fraction.  FP32 sums: a diagnostic, within about 1e-5 of exact.
+ * Errors: EINVAL (both or neither grad source, no code destination, one of
+ * the two monitor outputs, ...), EALIGN, ENODEV, ECUDA. */
 int fp8z1_step_fused(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float* grad_shard,
                      const float* const* d_grad_params, float* master_shard, float* m_shard,
                      float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
-                     float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
-                     const int32_t* d_found_inf, void* stream);
+                     float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0,
+                     int64_t b1, const double* d_sumsq, const int32_t* d_found_inf, void* stream);
+
+/* ---- param-wise split (§参数粒度切分; host only) ---------------------------- */
+
+/* The page's alternative to the block-wise split, for comparing padding
+ * waste: params sorted by size E*R*C, largest first (equal sizes keep their
+ * order), each given to the DP bucket with the fewest elements so far (lowest
+ * index on a tie); every bucket is then padded to the largest.  Writes
+ * owner[n_params] (the bucket of each param), bucket_elems[dp_size] (real
+ * elements per bucket) and, if not NULL, *padded_total = dp_size * largest
+ * bucket.  Host only; no CUDA call.  Errors: EINVAL. */
+int fp8z1_paramwise_split(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                          int32_t* owner, int64_t* bucket_elems, int64_t* padded_total);
+
+/* ---- MXFP8 variant (§Blockwise 量化: MXFP8; OCP MX specification v1.0) ----- */
+
+/* MXFP8 gives every run of 32 consecutive elements its own power-of-two
+ * (E8M0) scale, so a block never straddles rows of a weight whose C is a
+ * multiple of 32 and no fold is needed: the ZeRO shard is a flat run of the
+ * params' row-major elements, cut on group edges (the page's point that MXFP8
+ * blocks are memory-contiguous).  The MX layout holds the group count, the
+ * shard ranges and a small norm workspace.  Every C must be a multiple of 32
+ * (EINVAL otherwise).  Shard of rank r: S = ceil(n_groups / D) groups,
+ * [r*S, min((r+1)*S, n_groups)).  Flags as fp8z1_build_layout. */
+typedef struct fp8z1_mx_layout fp8z1_mx_layout;
+int fp8z1_mx_build_layout(const fp8z1_shape* shapes, int32_t n_params, int32_t dp_size,
+                          uint32_t flags, fp8z1_mx_layout** out);
+int fp8z1_mx_destroy_layout(fp8z1_mx_layout* layout);
+int fp8z1_mx_layout_info(const fp8z1_mx_layout* layout, int64_t* n_groups, int64_t* n_elems);
+int fp8z1_mx_shard_range(const fp8z1_mx_layout* layout, int32_t rank, int64_t* g0, int64_t* g1);
+
+/* fp8z1_grad_norm for a flat MX shard: adds the sum of squares of the
+ * (g1 - g0) * 32 FP32 grads at `grad_shard` (device, 16-byte aligned, at
+ * group g0) to *d_sumsq and ORs inf/nan into *d_found_inf; same reduction,
+ * accuracy and workspace rule.  Errors: EINVAL, EALIGN, ENODEV, ECUDA. */
+int fp8z1_mx_grad_norm(const fp8z1_mx_layout* layout, const float* grad_shard, int64_t g0, int64_t g1,
+                       double* d_sumsq, int32_t* d_found_inf, void* stream);
+
+/* The fused step on groups [g0, g1) of a flat MX shard: the unscale + clip +
+ * AdamW of fp8z1_step (same FP32 operations, same skip on found_inf), then per
+ * group of 32 the scale X = 2^(floor(log2 amax) - 8) clamped to
+ * 2^-127 .. 2^127 (X = 1 when amax == 0), written to scale_shard[g - g0] as
+ * the E8M0 code log2(X) + 127, and the codes E4M3(p / X), round to nearest
+ * even, saturating at 448, written to fp8_shard.  Pointers at group g0;
+ * grad/master/m/v/fp8 16-byte aligned.  Errors: EINVAL, EALIGN, ENODEV, ECUDA. */
+int fp8z1_mx_step(const fp8z1_mx_layout* layout, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                  float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                  uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
+                  const int32_t* d_found_inf, void* stream);
 
 /* ---- loss scaling (host; "DeepSpeed ZeRO 优化" §六, §九 Q6) ---------------- */
 

@@ -140,3 +140,41 @@ def test_scaler_matches_oracle_and_golden(row):
     assert [g[1] for g in got] == [int(x) for x in steps.split(",")]
     with pytest.raises(F.Fp8z1Error):
         F.fp8z1_scaler_update(F.fp8z1_loss_scaler(0.0, 0, 0, 1), 0)
+
+
+@pytest.mark.parametrize("dp", [1, 2, 3, 8])
+def test_paramwise_split_matches_oracle(dp):
+    for shapes in LUT_CASES + [synth.workload("dense").shapes, synth.workload("large").shapes]:
+        owner, bucket, padded = F.fp8z1_paramwise_split(shapes, dp)
+        o, b = oracle.paramwise_split(shapes, dp)
+        assert owner.tolist() == o.tolist() and bucket.tolist() == b.tolist()
+        assert padded == dp * int(b.max())
+
+
+@pytest.mark.parametrize("row", rows("paramwise_split.txt"), ids=lambda r: r[0])
+def test_paramwise_split_golden_through_abi(row):
+    sizes, dp, owner, buckets, padded = row
+    o, b, p = F.fp8z1_paramwise_split([(1, int(x), 1) for x in sizes.split(",")], int(dp))
+    assert o.tolist() == [int(x) for x in owner.split(",")]
+    assert b.tolist() == [int(x) for x in buckets.split(",")] and p == int(padded)
+
+
+def test_mx_layout_host():
+    shapes = synth.workload("moe").shapes + [(1, 1000, 3008)]
+    L = F.fp8z1_mx_build_layout(shapes, dp_size=8, host_only=True)
+    groups, elems = F.fp8z1_mx_layout_info(L)
+    assert elems == sum(e * r * c for e, r, c in shapes) and groups * 32 == elems
+    prev = 0
+    for r in range(8):
+        g0, g1 = F.fp8z1_mx_shard_range(L, r)
+        assert (g0, g1) == oracle.shard_range(groups, 8, r) and g0 == prev
+        prev = g1
+    assert prev == groups
+    with pytest.raises(F.Fp8z1Error):  # C not a multiple of 32
+        F.fp8z1_mx_build_layout([(1, 300, 200)], host_only=True)
+    lib = F.lib()
+    p = np.zeros(8, np.float64).ctypes.data
+    hp = F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1024.0, 1)
+    assert lib.fp8z1_mx_step(L.handle, C.byref(hp), p, p, p, p, p, p, 0, 1, p, p, None) == F.ENODEV
+    assert lib.fp8z1_mx_grad_norm(L.handle, p, 0, 1, p, p, None) == F.ENODEV
+    assert lib.fp8z1_mx_step(L.handle, C.byref(hp), p, p, p, p, p, p, 0, groups + 1, p, p, None) == F.EINVAL
