@@ -166,6 +166,14 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
 #pragma unroll
         for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
     } else {
+        if (s.vec && s.rows == FP8Z1_TILE && s.cols == FP8Z1_TILE) {
+            // a full, aligned block: chunk j sits 16 rows below chunk j-1
+            const float* src = s.tile + (int64_t)(tid >> 5) * s.ld + ((tid & 31) << 2);
+            const int64_t step = 16 * s.ld;
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) x[j] = __ldcs(reinterpret_cast<const float4*>(src + j * step));
+            return;
+        }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const int ci = tid + j * kThreads;
