@@ -271,20 +271,13 @@ def bench_ours(args, rank, world, dist):
             h.copy_(d)
         hfp8 = [torch.empty(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
         hscales = torch.empty(nblk, dtype=torch.float32, pin_memory=True)
-        hflag = torch.empty(1, dtype=torch.int32, pin_memory=True)
         h2d = sum(h.numel() * 4 for h in hgrads)
         d2h = sum(h.numel() for h in hfp8) + nblk * 4 + 4
 
         def e2e_step():
-            for d, h in zip(grads, hgrads):
-                d.copy_(h, non_blocking=True)
-            opt.launch_step(grads, fp8)
-            for h, d in zip(hfp8, fp8):
-                h.copy_(d, non_blocking=True)
-            hscales.copy_(opt.scales, non_blocking=True)
-            hflag.copy_(opt.found_inf, non_blocking=True)
-            torch.cuda.synchronize()
-            F.fp8z1_scaler_update(opt.scaler, int(hflag.item()))
+            # the public API's host path: chunked copies overlapped with the norm
+            # and the update (ShardOptimizer.step_from_host)
+            opt.step_from_host(hgrads, hfp8, hscales, grads=grads, fp8_params=fp8)
 
         e2e_step()
         if dist is not None:

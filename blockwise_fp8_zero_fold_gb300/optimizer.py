@@ -147,6 +147,93 @@ class ShardOptimizer:
         if fp8_params is not None:
             self.unfold_from(self.codes, fp8_params, stream)
 
+    # -- host-resident grads and FP8 weights ----------------------------------
+    def _host_chunks(self, target_blocks: int):
+        """Contiguous block ranges of this shard whose grads are contiguous rows
+        of one param (one expert, or a run of row blocks of a 2-D weight), read
+        off the library's block table: (param, expert, row0, row1, k0, k1)."""
+        lut = F.fp8z1_copy_lut(self.layout)[self.b0:self.b1]
+        out = []
+        k = 0
+        n = len(lut)
+        while k < n:
+            p, e, rb = int(lut["param"][k]), int(lut["expert"][k]), int(lut["row_block"][k])
+            j = k
+            while (j < n and int(lut["param"][j]) == p and int(lut["expert"][j]) == e
+                   and (j - k < target_blocks or int(lut["row_block"][j]) == int(lut["row_block"][j - 1]))):
+                j += 1
+            rb_last = int(lut["row_block"][j - 1])
+            rows_last = int(lut["rows_real"][j - 1])
+            out.append((p, e, 128 * rb, 128 * rb_last + rows_last, self.b0 + k, self.b0 + j))
+            k = j
+        return out
+
+    def step_from_host(self, host_grads: Sequence[torch.Tensor], host_fp8: Sequence[torch.Tensor],
+                       host_scales: Optional[torch.Tensor] = None, grads: Optional[Sequence[torch.Tensor]] = None,
+                       fp8_params: Optional[Sequence[torch.Tensor]] = None, target_blocks: int = 1792) -> int:
+        """One step whose grads arrive from (pinned) host memory and whose FP8
+        weights (and scales) go back to it, with the copies overlapped: chunk
+        c's grads are copied on a copy stream while chunk c-1's norm runs, and
+        after the norm chunk c's update runs while chunk c-1's FP8 weights are
+        copied back.  ``grads`` / ``fp8_params`` are the device tensors used
+        (allocated on first use when not given).  Fused path, whole-buffer
+        shards only: the copies move whole rows, and a shard that starts or
+        ends inside a row of blocks would copy back rows it did not update.
+        Host tensors should be pinned for the copies to overlap."""
+        assert self.fused, "step_from_host runs the fused path"
+        if (self.b0, self.b1) != (0, self.nblk):
+            raise ValueError("step_from_host needs the whole buffer as the shard (dp_size 1)")
+        if grads is None:
+            grads = getattr(self, "_dev_grads", None) or [torch.empty(s, dtype=torch.float32, device=self.device)
+                                                          for s in self.shapes]
+            self._dev_grads = grads
+        if fp8_params is None:
+            fp8_params = getattr(self, "_dev_fp8", None) or [torch.empty(s, dtype=torch.uint8, device=self.device)
+                                                             for s in self.shapes]
+            self._dev_fp8 = fp8_params
+        if getattr(self, "_chunks_cache", None) is None or self._chunks_cache[0] != target_blocks:
+            self._chunks_cache = (target_blocks, self._host_chunks(target_blocks))
+            self._copy_in = torch.cuda.Stream(self.device)
+            self._copy_out = torch.cuda.Stream(self.device)
+            self._flag = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        chunks = self._chunks_cache[1]
+        comp = torch.cuda.current_stream(self.device)
+        gptrs, fptrs = self._ptrs(grads), self._ptrs(fp8_params)
+        self.sumsq.zero_()
+        self.found_inf.zero_()
+        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
+        ready = []
+        for p, e, r0, r1, k0, k1 in chunks:  # grads in, norm as each chunk lands
+            ev = torch.cuda.Event()
+            with torch.cuda.stream(self._copy_in):
+                grads[p][e, r0:r1].copy_(host_grads[p][e, r0:r1], non_blocking=True)
+                ev.record(self._copy_in)
+            comp.wait_event(ev)
+            F.fp8z1_fold_norm(self.layout, gptrs, None, k0, k1, self.sumsq, self.found_inf, comp)
+        if self.norm_hook is not None:
+            self.norm_hook(self.sumsq, self.found_inf)
+        for p, e, r0, r1, k0, k1 in chunks:  # update, FP8 weights out as each chunk is done
+            F.fp8z1_step_fused(self.layout, hp, d_grad_params=gptrs, master_shard=self.master[(k0 - self.b0) * F.BLOCK_ELEMS:],
+                               m_shard=self.m[(k0 - self.b0) * F.BLOCK_ELEMS:], v_shard=self.v[(k0 - self.b0) * F.BLOCK_ELEMS:],
+                               d_fp8_params=fptrs, scale_shard=self.scales[k0 - self.b0:], b0=k0, b1=k1,
+                               d_sumsq=self.sumsq, d_found_inf=self.found_inf, stream=comp)
+            ev = torch.cuda.Event()
+            ev.record(comp)
+            self._copy_out.wait_event(ev)
+            with torch.cuda.stream(self._copy_out):
+                host_fp8[p][e, r0:r1].copy_(fp8_params[p][e, r0:r1], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(comp)
+        self._copy_out.wait_event(ev)
+        with torch.cuda.stream(self._copy_out):
+            if host_scales is not None:
+                host_scales.copy_(self.scales, non_blocking=True)
+            self._flag.copy_(self.found_inf, non_blocking=True)
+        self._copy_out.synchronize()
+        found = int(self._flag.item())
+        F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
     def finish_step(self) -> int:
         """Read found_inf (synchronises) and update the loss scale and t."""
         found = int(self.found_inf.item())

@@ -55,3 +55,39 @@ def test_resume_is_bit_identical(lib):
     assert ref.scaler.step == 4  # one of the five steps was skipped
     with pytest.raises(ValueError):
         _make(synth.workload("tiny"), 0).load_state_dict(ref.state_dict())
+
+
+@pytest.mark.parametrize("max_norm", [1e30, 0.05])
+def test_step_from_host_matches_device_path(lib, max_norm):
+    """Grads from pinned host memory and FP8 weights back to it, with the
+    copies overlapped: the same state as the device-resident step.  With
+    clipping off the result is bit-identical; with clipping on the chunked
+    norm adds its partials in another order, so 1e-6 relative."""
+    w = synth.workload("tiny", shapes=[(3, 512, 384), (1, 1000, 131)], dp=1, rank=0,
+                       m_sigma=1e-4, v_sigma=1e-8, max_norm=max_norm)
+    ref = _make(w, 0)
+    host = _make(w, 0)
+    for o in (ref, host):
+        o.init_state(*(synth.make_state(w, k, "cuda") for k in ("master", "m", "v")))
+    fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w.shapes]
+    hfp8 = [torch.zeros(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
+    hsc = torch.zeros(host.nblk, dtype=torch.float32, pin_memory=True)
+    for t in (1, 2):
+        g = synth.make_grads(w, t, "cuda")
+        hg = [x.cpu().pin_memory() for x in g]
+        assert ref.step(g, fp8) == 0
+        assert host.step_from_host(hg, hfp8, hsc, target_blocks=7) == 0
+    torch.cuda.synchronize()
+    for name in ("master", "m", "v", "scales"):
+        a, b = getattr(ref, name), getattr(host, name)
+        if max_norm > 1e20:
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
+        else:
+            assert torch.allclose(a, b, rtol=1e-6, atol=0), name
+    if max_norm > 1e20:
+        for a, b in zip(fp8, hfp8):
+            assert torch.equal(a.cpu(), b)
+        assert torch.equal(hsc, ref.scales.cpu())
+    assert host.scaler.step == 2
+    with pytest.raises(ValueError):
+        _make(synth.workload("tiny"), 0).step_from_host([], [])
