@@ -13,6 +13,7 @@ newer) with ``gcc -std=c11 -O2 -ffp-contract=off``.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import os
 import subprocess
@@ -66,12 +67,10 @@ class ScalerState(C.Structure):
                 ("growth_interval", C.c_int32)]
 
 
-def lib():
-    global _lib
-    with _lock:
-        if _lib is None:
-            build()
-            L = C.CDLL(_LIB)
+def _bind(L):
+    """Declare the C signatures on a loaded oracle library."""
+    if True:
+        if True:
             P = C.c_void_p
             i64, i32 = C.c_int64, C.c_int32
             L.oracle_count_blocks.argtypes = [C.POINTER(Shape), i32]
@@ -109,8 +108,32 @@ def lib():
             L.oracle_mx_quantise_group.argtypes = [P, P, P]
             L.oracle_mx_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
             L.oracle_mx_step.restype = C.c_int
-            _lib = L
+    return L
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(C.CDLL(_LIB))
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Run this front against another build of the oracle for a while (the
+    tests use it to plant mistakes in a copy and check that the pins fail)."""
+    global _lib
+    lib()
+    with _lock:
+        old = _lib
+        _lib = _bind(C.CDLL(path))
+    try:
+        yield
+    finally:
+        with _lock:
+            _lib = old
 
 
 # ---------------------------------------------------------------------------
