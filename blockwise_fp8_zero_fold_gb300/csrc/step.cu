@@ -329,10 +329,11 @@ struct MxArgs {
 
 // Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
 // u, its 32 lanes hold 4 whole groups) and issues every load of them before
-// any update, so four chunks' loads are in flight per thread.
-constexpr int kMxUnroll = 4;
+// any update; with 3 CTAs resident per SM (24 warps) that keeps about 96 KB
+// of loads in flight per SM.
+constexpr int kMxUnroll = 2;
 
-__global__ void __launch_bounds__(kMxThreads) mx_step_kernel(const MxArgs a)
+__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
@@ -566,8 +567,8 @@ extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp,
     a.found_inf = d_found_inf;
     a.n_chunks = chunks;
     a.c = scalars(hp);
-    // a persistent grid: 4 CTAs of 256 threads per SM, no more than the chunks need
-    int64_t grid = (int64_t)L->sm_count * 4;
+    // a persistent grid: 8 CTAs of 256 threads per SM (3 resident), no more than the chunks need
+    int64_t grid = (int64_t)L->sm_count * 8;
     const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
     if (grid > need) grid = need;
     mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
