@@ -1,0 +1,137 @@
+// The fused optimizer step of the MXFP8 variant.
+//
+// "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §Blockwise 量化: MXFP8 is the
+// Blackwell format that gives every memory-contiguous block its own E8M0
+// scale (OCP Microscaling specification v1.0); §Blockwise 量化给 ZeRO-1 带来的
+// 挑战: such blocks survive a flat ZeRO split, so no fold is needed.  The
+// shard is a flat run of the params' row-major elements; a group of 32
+// consecutive values shares the scale X = 2^(floor(log2 amax) - 8), clamped to
+// 2^-127 .. 2^127 (X = 1 when amax = 0), stored as the E8M0 code
+// log2(X) + 127, and each value becomes E4M3(p / X), rounded to nearest even
+// and saturated at 448.  The update is update.cuh's, bit for bit the
+// block-wise one.  There is no table and no CTA barrier: a group is 8
+// consecutive lanes (one float4 each), its amax three shuffles.
+#include "update.cuh"
+
+namespace {
+
+using namespace fp8z1;
+
+constexpr int kMxThreads = 256;
+struct MxArgs {
+    const float4* grad;
+    float4* master;
+    float4* mom1;
+    float4* mom2;
+    uint32_t* codes;
+    uint8_t* scales;   // one E8M0 code per group
+    const double* sumsq;
+    const int32_t* found_inf;
+    int64_t n_chunks;  // float4 chunks: 8 per group
+    StepScalars c;
+};
+
+// Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
+// u, its 32 lanes hold 4 whole groups) and issues every load of them before
+// any update; with 3 CTAs resident per SM (24 warps) that keeps about 96 KB
+// of loads in flight per SM.
+constexpr int kMxUnroll = 2;
+
+__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
+{
+    if (*a.found_inf != 0) return;  // skipped step: write nothing
+    __shared__ float s_gscale;
+    if (threadIdx.x == 0) s_gscale = grad_factor(*a.sumsq, a.c);
+    __syncthreads();
+    const float gs = s_gscale;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kMxThreads / 32);
+    // the trip count is uniform across a warp, so the group shuffles always see
+    // all 32 lanes; a group's 8 lanes are in or out of range together
+    for (int64_t wbase = warp * (32 * kMxUnroll); wbase < a.n_chunks; wbase += nwarps * (32 * kMxUnroll)) {
+        float4 g4[kMxUnroll], p4[kMxUnroll], m4[kMxUnroll], v4[kMxUnroll];
+#pragma unroll
+        for (int u = 0; u < kMxUnroll; ++u) {
+            const int64_t i = wbase + u * 32 + lane;
+            if (i < a.n_chunks) {
+                g4[u] = __ldcs(a.grad + i);
+                p4[u] = a.master[i];
+                m4[u] = a.mom1[i];
+                v4[u] = a.mom2[i];
+            } else {
+                g4[u] = p4[u] = m4[u] = v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMxUnroll; ++u) {
+            const int64_t i = wbase + u * 32 + lane;
+            const bool valid = i < a.n_chunks;
+            if (valid) {
+                adamw(gs, a.c, g4[u].x, p4[u].x, m4[u].x, v4[u].x);
+                adamw(gs, a.c, g4[u].y, p4[u].y, m4[u].y, v4[u].y);
+                adamw(gs, a.c, g4[u].z, p4[u].z, m4[u].z, v4[u].z);
+                adamw(gs, a.c, g4[u].w, p4[u].w, m4[u].w, v4[u].w);
+                __stcs(a.mom1 + i, m4[u]);
+                __stcs(a.mom2 + i, v4[u]);
+                __stcs(a.master + i, p4[u]);
+            }
+            const float4 p = p4[u];
+            float amax = fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w)));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+            // floor(log2 amax) - 8 from the exponent field (a subnormal amax has
+            // field 0 and clamps to -127); 2^-s is then a normal float
+            int sexp = 0;
+            if (amax != 0.0f) {
+                sexp = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 8;
+                sexp = sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
+            }
+            const float inv = __uint_as_float((uint32_t)(127 - sexp) << 23);
+            const uint32_t lo = e4m3x2(__fmul_rn(p.x, inv), __fmul_rn(p.y, inv));
+            const uint32_t hi = e4m3x2(__fmul_rn(p.z, inv), __fmul_rn(p.w, inv));
+            if (valid) {
+                __stcs(a.codes + i, lo | (hi << 16));
+                if ((lane & 7) == 0) a.scales[i >> 3] = (uint8_t)(sexp + 127);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                             float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                             uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
+                             const int32_t* d_found_inf, void* stream)
+{
+    if (!L || !hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
+        !d_sumsq || !d_found_inf || !in_domain(hp))
+        return FP8Z1_EINVAL;
+    if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(master_shard, 16) || !fp8z1::aligned(m_shard, 16) ||
+        !fp8z1::aligned(v_shard, 16) || !fp8z1::aligned(fp8_shard, 16) || !fp8z1::aligned(d_sumsq, 8) ||
+        !fp8z1::aligned(d_found_inf, 4))
+        return FP8Z1_EALIGN;
+    const int64_t chunks = (g1 - g0) * (FP8Z1_MX_GROUP / 4);
+    if (chunks == 0) return FP8Z1_OK;
+    MxArgs a = {};
+    a.grad = reinterpret_cast<const float4*>(grad_shard);
+    a.master = reinterpret_cast<float4*>(master_shard);
+    a.mom1 = reinterpret_cast<float4*>(m_shard);
+    a.mom2 = reinterpret_cast<float4*>(v_shard);
+    a.codes = reinterpret_cast<uint32_t*>(fp8_shard);
+    a.scales = scale_shard;
+    a.sumsq = d_sumsq;
+    a.found_inf = d_found_inf;
+    a.n_chunks = chunks;
+    a.c = scalars(hp);
+    // a persistent grid: 8 CTAs of 256 threads per SM (3 resident), no more than the chunks need
+    int64_t grid = (int64_t)L->sm_count * 8;
+    const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
+    if (grid > need) grid = need;
+    mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    return fp8z1::launch_status();
+}

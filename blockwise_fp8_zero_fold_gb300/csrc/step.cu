@@ -26,27 +26,19 @@
 //                lookup table (the unfold of the codes, fused);
 //   CODES_FOLDED codes are written to the folded code shard.
 //
-// FP32 operation order per element (no contraction beyond the explicit fmas;
-// division and square root correctly rounded):
-//   g   = g_s * gscale,  gscale = (clip_coef < 1 ? (float)clip_coef : 1) / S
-//   m   = fma(beta1, m, (1-beta1) * g)
-//   v   = fma(beta2, v, ((1-beta2) * g) * g)
-//   den = fma(sqrt(v), 1/sqrt(1-beta2^t), eps)
-//   p   = fma(-lr/(1-beta1^t), m / den, p * (1 - lr*wd))
-// scale = amax/448 (1 when amax == 0); code = cvt.rn.satfinite.e4m3(p / scale).
+// The FP32 update is update.cuh's; then scale = amax/448 (1 when amax == 0)
+// and code = cvt.rn.satfinite.e4m3(p / scale).
 #include <math.h>
 
-#include "internal.h"
+#include "update.cuh"
 
 namespace {
+
+using namespace fp8z1;
 
 constexpr int kThreads = 512;
 constexpr int kVec = FP8Z1_BLOCK_ELEMS / 4 / kThreads;  // 8 float4 per thread
 constexpr int kWarps = kThreads / 32;
-
-struct StepScalars {
-    float beta1, beta2, omb1, omb2, eps, step_size, inv_sqrt_bc2, decay, max_norm, loss_scale;
-};
 
 struct StepArgs {
     const float4* grad;          // folded grad shard (!GRAD_ROWS)
@@ -66,36 +58,6 @@ struct StepArgs {
     uint32_t* block_underflow;   // MON: non-zero masters whose code is 0, per block
     StepScalars c;
 };
-
-__device__ __forceinline__ void adamw(float gs, const StepScalars& c, float g_s, float& p, float& m,
-                                      float& v)
-{
-    const float g = __fmul_rn(g_s, gs);
-    m = __fmaf_rn(c.beta1, m, __fmul_rn(c.omb1, g));
-    v = __fmaf_rn(c.beta2, v, __fmul_rn(__fmul_rn(c.omb2, g), g));
-    const float den = __fmaf_rn(__fsqrt_rn(v), c.inv_sqrt_bc2, c.eps);
-    p = __fmaf_rn(-c.step_size, __fdiv_rn(m, den), __fmul_rn(p, c.decay));
-}
-
-// two floats -> two E4M3 codes (lo in the low byte), round to nearest even,
-// finite overflow saturated to +-448
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
-{
-    unsigned short r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// two E4M3 codes (low byte -> .x) -> their exact values
-__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two)
-{
-    uint32_t h2;
-    asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h2) : "r"(two));
-    float lo, hi;
-    asm("{ .reg .b16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
-    return make_float2(lo, hi);
-}
 
 __device__ __forceinline__ float warp_max(float v)
 {
@@ -160,12 +122,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        const double global = sqrt(*a.sumsq) / (double)a.c.loss_scale;
-        const double coef = (double)a.c.max_norm / (global + 1e-6);
-        const float clip = coef < 1.0 ? (float)coef : 1.0f;
-        s_gscale = __fdiv_rn(clip, a.c.loss_scale);
-    }
+    if (tid == 0) s_gscale = grad_factor(*a.sumsq, a.c);
 
     // the block's place in its row-major param (only for the row-major forms)
     int rows = 0, cols = 0;
@@ -302,132 +259,6 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     }
 }
 
-// ---------------------------------------------------------------------------
-// MXFP8 ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §Blockwise 量化: the
-// Blackwell format that gives every memory-contiguous block its own E8M0
-// scale; OCP MX specification v1.0).  The shard is a flat run of the params'
-// row-major elements; a group of 32 consecutive values shares the scale
-// X = 2^(floor(log2 amax) - 8), clamped to 2^-127 .. 2^127 (X = 1 when
-// amax = 0), stored as the E8M0 code log2(X) + 127, and each value becomes
-// E4M3(p / X), rounded to nearest even and saturated at 448.  Because the
-// groups are contiguous there is no fold, no table and no block barrier: a
-// group is 8 consecutive lanes (one float4 each), its amax three shuffles.
-constexpr int kMxThreads = 256;
-
-struct MxArgs {
-    const float4* grad;
-    float4* master;
-    float4* mom1;
-    float4* mom2;
-    uint32_t* codes;
-    uint8_t* scales;   // one E8M0 code per group
-    const double* sumsq;
-    const int32_t* found_inf;
-    int64_t n_chunks;  // float4 chunks: 8 per group
-    StepScalars c;
-};
-
-// Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
-// u, its 32 lanes hold 4 whole groups) and issues every load of them before
-// any update; with 3 CTAs resident per SM (24 warps) that keeps about 96 KB
-// of loads in flight per SM.
-constexpr int kMxUnroll = 2;
-
-__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
-{
-    if (*a.found_inf != 0) return;  // skipped step: write nothing
-    __shared__ float s_gscale;
-    if (threadIdx.x == 0) {
-        const double global = sqrt(*a.sumsq) / (double)a.c.loss_scale;
-        const double coef = (double)a.c.max_norm / (global + 1e-6);
-        const float clip = coef < 1.0 ? (float)coef : 1.0f;
-        s_gscale = __fdiv_rn(clip, a.c.loss_scale);
-    }
-    __syncthreads();
-    const float gs = s_gscale;
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kMxThreads / 32);
-    // the trip count is uniform across a warp, so the group shuffles always see
-    // all 32 lanes; a group's 8 lanes are in or out of range together
-    for (int64_t wbase = warp * (32 * kMxUnroll); wbase < a.n_chunks; wbase += nwarps * (32 * kMxUnroll)) {
-        float4 g4[kMxUnroll], p4[kMxUnroll], m4[kMxUnroll], v4[kMxUnroll];
-#pragma unroll
-        for (int u = 0; u < kMxUnroll; ++u) {
-            const int64_t i = wbase + u * 32 + lane;
-            if (i < a.n_chunks) {
-                g4[u] = __ldcs(a.grad + i);
-                p4[u] = a.master[i];
-                m4[u] = a.mom1[i];
-                v4[u] = a.mom2[i];
-            } else {
-                g4[u] = p4[u] = m4[u] = v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kMxUnroll; ++u) {
-            const int64_t i = wbase + u * 32 + lane;
-            const bool valid = i < a.n_chunks;
-            if (valid) {
-                adamw(gs, a.c, g4[u].x, p4[u].x, m4[u].x, v4[u].x);
-                adamw(gs, a.c, g4[u].y, p4[u].y, m4[u].y, v4[u].y);
-                adamw(gs, a.c, g4[u].z, p4[u].z, m4[u].z, v4[u].z);
-                adamw(gs, a.c, g4[u].w, p4[u].w, m4[u].w, v4[u].w);
-                __stcs(a.mom1 + i, m4[u]);
-                __stcs(a.mom2 + i, v4[u]);
-                __stcs(a.master + i, p4[u]);
-            }
-            const float4 p = p4[u];
-            float amax = fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(p.z), fabsf(p.w)));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-            // floor(log2 amax) - 8 from the exponent field (a subnormal amax has
-            // field 0 and clamps to -127); 2^-s is then a normal float
-            int sexp = 0;
-            if (amax != 0.0f) {
-                sexp = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127 - 8;
-                sexp = sexp < -127 ? -127 : (sexp > 127 ? 127 : sexp);
-            }
-            const float inv = __uint_as_float((uint32_t)(127 - sexp) << 23);
-            const uint32_t lo = e4m3x2(__fmul_rn(p.x, inv), __fmul_rn(p.y, inv));
-            const uint32_t hi = e4m3x2(__fmul_rn(p.z, inv), __fmul_rn(p.w, inv));
-            if (valid) {
-                __stcs(a.codes + i, lo | (hi << 16));
-                if ((lane & 7) == 0) a.scales[i >> 3] = (uint8_t)(sexp + 127);
-            }
-        }
-    }
-}
-
-bool in_domain(const fp8z1_adamw_hp* hp)
-{
-    return hp->step >= 1 && hp->lr >= 0.0f && hp->beta1 >= 0.0f && hp->beta1 < 1.0f &&
-           hp->beta2 >= 0.0f && hp->beta2 < 1.0f && hp->eps > 0.0f && hp->weight_decay >= 0.0f &&
-           hp->max_norm > 0.0f && hp->loss_scale > 0.0f && isfinite(hp->loss_scale) &&
-           isfinite(hp->lr) && isfinite(hp->eps) && isfinite(hp->weight_decay);
-}
-
-// per-step scalars, in double on the host, rounded once to FP32
-StepScalars scalars(const fp8z1_adamw_hp* hp)
-{
-    const double t = (double)hp->step;
-    const double bc1 = 1.0 - pow((double)hp->beta1, t);
-    const double bc2 = 1.0 - pow((double)hp->beta2, t);
-    StepScalars c;
-    c.beta1 = hp->beta1;
-    c.beta2 = hp->beta2;
-    c.omb1 = (float)(1.0 - (double)hp->beta1);
-    c.omb2 = (float)(1.0 - (double)hp->beta2);
-    c.eps = hp->eps;
-    c.step_size = (float)((double)hp->lr / bc1);
-    c.inv_sqrt_bc2 = (float)(1.0 / sqrt(bc2));
-    c.decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);
-    c.max_norm = hp->max_norm;
-    c.loss_scale = hp->loss_scale;
-    return c;
-}
-
 int check_common(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* master, const float* m,
                  const float* v, const float* scales, int64_t b0, int64_t b1, const double* d_sumsq,
                  const int32_t* d_found_inf)
@@ -537,40 +368,5 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
         else if (cr) launch_mon<false, true, false>(a, nb, s, mon);
         else launch_mon<false, false, true>(a, nb, s, mon);
     }
-    return fp8z1::launch_status();
-}
-
-extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
-                             float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
-                             uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
-                             const int32_t* d_found_inf, void* stream)
-{
-    if (!L || !hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
-        !d_sumsq || !d_found_inf || !in_domain(hp))
-        return FP8Z1_EINVAL;
-    if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
-    if (!L->on_device) return FP8Z1_ENODEV;
-    if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(master_shard, 16) || !fp8z1::aligned(m_shard, 16) ||
-        !fp8z1::aligned(v_shard, 16) || !fp8z1::aligned(fp8_shard, 16) || !fp8z1::aligned(d_sumsq, 8) ||
-        !fp8z1::aligned(d_found_inf, 4))
-        return FP8Z1_EALIGN;
-    const int64_t chunks = (g1 - g0) * (FP8Z1_MX_GROUP / 4);
-    if (chunks == 0) return FP8Z1_OK;
-    MxArgs a = {};
-    a.grad = reinterpret_cast<const float4*>(grad_shard);
-    a.master = reinterpret_cast<float4*>(master_shard);
-    a.mom1 = reinterpret_cast<float4*>(m_shard);
-    a.mom2 = reinterpret_cast<float4*>(v_shard);
-    a.codes = reinterpret_cast<uint32_t*>(fp8_shard);
-    a.scales = scale_shard;
-    a.sumsq = d_sumsq;
-    a.found_inf = d_found_inf;
-    a.n_chunks = chunks;
-    a.c = scalars(hp);
-    // a persistent grid: 8 CTAs of 256 threads per SM (3 resident), no more than the chunks need
-    int64_t grid = (int64_t)L->sm_count * 8;
-    const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
-    if (grid > need) grid = need;
-    mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
