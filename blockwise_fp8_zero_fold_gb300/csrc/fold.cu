@@ -140,6 +140,7 @@ int check(const fp8z1_layout* L, const void* params, const void* shard, int32_t 
 extern "C" int fp8z1_fold(const fp8z1_layout* L, const void* const* d_src_params, void* dst_shard,
                           int32_t elem_size, int64_t b0, int64_t b1, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_fold");
     const int st = check(L, d_src_params, dst_shard, elem_size, b0, b1);
     if (st != FP8Z1_OK || b0 == b1) return st;
     return launch<true>(L, const_cast<void* const*>(d_src_params), static_cast<uint8_t*>(dst_shard),
@@ -149,6 +150,7 @@ extern "C" int fp8z1_fold(const fp8z1_layout* L, const void* const* d_src_params
 extern "C" int fp8z1_unfold(const fp8z1_layout* L, const void* src_shard, void* const* d_dst_params,
                             int32_t elem_size, int64_t b0, int64_t b1, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_unfold");
     const int st = check(L, d_dst_params, src_shard, elem_size, b0, b1);
     if (st != FP8Z1_OK || b0 == b1) return st;
     return launch<false>(L, d_dst_params, const_cast<uint8_t*>(static_cast<const uint8_t*>(src_shard)),

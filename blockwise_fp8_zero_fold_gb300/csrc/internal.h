@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <vector>
@@ -44,6 +45,29 @@ struct fp8z1_mx_layout {
 };
 
 namespace fp8z1 {
+
+// NVTX ranges around the device entry points, in their own "fp8z1" domain
+// (a no-op unless a profiler attaches; ranges of other domains are unaffected).
+inline nvtxDomainHandle_t nvtx_domain()
+{
+    static nvtxDomainHandle_t d = nvtxDomainCreateA("fp8z1");
+    return d;
+}
+
+struct NvtxRange {
+    explicit NvtxRange(const char* name)
+    {
+        nvtxEventAttributes_t e = {};
+        e.version = NVTX_VERSION;
+        e.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        e.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        e.message.ascii = name;
+        nvtxDomainRangePushEx(nvtx_domain(), &e);
+    }
+    ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -6,6 +6,7 @@
 // block's param and real extent, and ZeRO shards are cut on block edges;
 // §参数布局变换: block order of fold is (expert, row block, col block).
 #include <limits.h>
+#include <math.h>
 
 #include <algorithm>
 #include <new>
@@ -219,6 +220,18 @@ extern "C" int fp8z1_paramwise_split(const fp8z1_shape* shapes, int32_t n_params
         for (int32_t b = 0; b < dp_size; ++b) mx = bucket_elems[b] > mx ? bucket_elems[b] : mx;
         *padded_total = mx * dp_size;
     }
+    return FP8Z1_OK;
+}
+
+// "DeepSpeed ZeRO 优化" §七: the clip arithmetic the step kernels perform on
+// the device, on the host, for logging.
+extern "C" int fp8z1_clip_coef(double sumsq, float max_norm, float loss_scale, double* global_norm,
+                               double* clip_coef)
+{
+    if (!global_norm || !clip_coef || !(loss_scale > 0.0f) || !(max_norm > 0.0f) || !(sumsq >= 0.0))
+        return FP8Z1_EINVAL;
+    *global_norm = sqrt(sumsq) / (double)loss_scale;
+    *clip_coef = (double)max_norm / (*global_norm + 1e-6);
     return FP8Z1_OK;
 }
 

@@ -106,6 +106,7 @@ extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp,
                              uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
                              const int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_mx_step");
     if (!L || !hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
         !d_sumsq || !d_found_inf || !in_domain(hp))
         return FP8Z1_EINVAL;

@@ -303,6 +303,7 @@ int64_t persistent_grid(const fp8z1_layout* L, int64_t n)
 extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, int64_t b0, int64_t b1,
                                double* d_sumsq, int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_grad_norm");
     if (!grad_shard || !d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
     const int st = fp8z1::check_range(L, b0, b1);
     if (st != FP8Z1_OK) return st;
@@ -327,6 +328,7 @@ extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, i
 extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad_params, float* grad_shard,
                                int64_t b0, int64_t b1, double* d_sumsq, int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_fold_norm");
     if (!d_grad_params || !d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
     const int st = fp8z1::check_range(L, b0, b1);
     if (st != FP8Z1_OK) return st;
@@ -361,6 +363,7 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
 extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_shard, int64_t g0,
                                   int64_t g1, double* d_sumsq, int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_mx_grad_norm");
     if (!L || !grad_shard || !d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
     if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
     if (!L->on_device) return FP8Z1_ENODEV;

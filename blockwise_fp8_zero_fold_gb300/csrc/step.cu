@@ -296,6 +296,7 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
                           float* scale_shard, int64_t b0, int64_t b1, const double* d_sumsq,
                           const int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_step");
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
     if (st != FP8Z1_OK) return st;
     if (!grad_shard || !fp8_shard) return FP8Z1_EINVAL;
@@ -325,6 +326,7 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
                                 int64_t b0, int64_t b1, const double* d_sumsq,
                                 const int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_step_fused");
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
     if (st != FP8Z1_OK) return st;
     // exactly one grad source, at least one code destination

@@ -92,6 +92,8 @@ _SIGS = {
     "fp8z1_mx_step": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, C.c_int64,
                                 C.c_int64, _P, _P, _P]),
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
+    "fp8z1_clip_coef": (C.c_int, [C.c_double, C.c_float, C.c_float, C.POINTER(C.c_double),
+                                  C.POINTER(C.c_double)]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
 
@@ -340,6 +342,14 @@ def fp8z1_mx_step(layout: MxLayout, hp: fp8z1_adamw_hp, grad_shard, master_shard
                                _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard), _ptr(scale_shard),
                                int(g0), int(g1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_mx_step")
+
+
+def fp8z1_clip_coef(sumsq: float, max_norm: float, loss_scale: float):
+    """(global_norm, clip_coef) of a step, as the device computes them."""
+    g, c = C.c_double(), C.c_double()
+    _check(lib().fp8z1_clip_coef(float(sumsq), float(max_norm), float(loss_scale), C.byref(g), C.byref(c)),
+           "fp8z1_clip_coef")
+    return g.value, c.value
 
 
 def fp8z1_scaler_update(scaler: fp8z1_loss_scaler, found_inf: int):

@@ -244,6 +244,18 @@ class ShardOptimizer:
         self.launch_step(grads, fp8_params, stream)
         return self.finish_step()
 
+    def stats(self, loss_scale: Optional[float] = None) -> dict:
+        """Numbers for logging the last step (reads two device scalars): the
+        global grad norm and clip coefficient (on this shard's sum of squares,
+        after any norm hook), the loss scale the step used (pass it when the
+        scaler has moved since), t and S now, and whether it was skipped."""
+        s = float(self.sumsq.item())
+        found = int(self.found_inf.item())
+        used = self.scaler.scale if loss_scale is None else loss_scale
+        norm, coef = (float("nan"), float("nan")) if found else F.fp8z1_clip_coef(s, self.hp["max_norm"], used)
+        return {"global_norm": norm, "clip_coef": coef, "clipped": bool(not found and coef < 1.0),
+                "skipped": bool(found), "loss_scale": self.scaler.scale, "step": self.scaler.step}
+
 
 class MxShardOptimizer:
     """The same optimizer step with MXFP8 weights (E8M0 scale per 32

@@ -326,6 +326,14 @@ int fp8z1_mx_step(const fp8z1_mx_layout* layout, const fp8z1_adamw_hp* hp, const
  * Host only.  Errors: EINVAL (null, scale <= 0, growth_interval < 1). */
 int fp8z1_scaler_update(fp8z1_loss_scaler* scaler, int32_t found_inf);
 
+/* The clip arithmetic the step kernels perform on the device ("DeepSpeed ZeRO
+ * 优化" §七), on the host, for logging a step: global_norm = sqrt(sumsq) /
+ * loss_scale and clip_coef = max_norm / (global_norm + 1e-6), in double; the
+ * step applies clip_coef when it is < 1.  Host only.  Errors: EINVAL (null
+ * outputs, sumsq < 0 or nan, loss_scale or max_norm <= 0). */
+int fp8z1_clip_coef(double sumsq, float max_norm, float loss_scale, double* global_norm,
+                    double* clip_coef);
+
 /* Static text for a status code. */
 const char* fp8z1_strerror(int status);
 

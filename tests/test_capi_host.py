@@ -178,3 +178,15 @@ def test_mx_layout_host():
     assert lib.fp8z1_mx_step(L.handle, C.byref(hp), p, p, p, p, p, p, 0, 1, p, p, None) == F.ENODEV
     assert lib.fp8z1_mx_grad_norm(L.handle, p, 0, 1, p, p, None) == F.ENODEV
     assert lib.fp8z1_mx_step(L.handle, C.byref(hp), p, p, p, p, p, p, 0, groups + 1, p, p, None) == F.EINVAL
+
+
+@pytest.mark.parametrize("row", rows("clip_example.txt"))
+def test_clip_coef_host_matches_oracle_and_golden(row):
+    max_norm, S, grads, sumsq, gnorm, coef, applies, clipped = row
+    g, c = F.fp8z1_clip_coef(float(sumsq), float(max_norm), float(S))
+    og, oc, oa = oracle.clip_coef(float(sumsq), float(max_norm), float(S))
+    assert (g, c) == (og, oc)
+    assert g == float(gnorm) and c == pytest.approx(float(coef), rel=1e-15)
+    assert (c < 1.0) == bool(int(applies))
+    with pytest.raises(F.Fp8z1Error):
+        F.fp8z1_clip_coef(-1.0, 1.0, 1.0)

@@ -4,6 +4,8 @@ buffers plus t and S; the norm reduction is deterministic, so resuming
 reproduces every bit."""
 import io
 
+import numpy as np
+
 import pytest
 import torch
 
@@ -91,3 +93,18 @@ def test_step_from_host_matches_device_path(lib, max_norm):
     assert host.scaler.step == 2
     with pytest.raises(ValueError):
         _make(synth.workload("tiny"), 0).step_from_host([], [])
+
+
+def test_stats_report_the_step(lib):
+    import oracle
+    w = synth.workload("tiny", dp=1, rank=0, max_norm=0.05)
+    opt = _make(w, 0)
+    opt.init_state(synth.make_state(w, "master", "cuda"))
+    g = synth.make_grads(w, 1, "cuda")
+    assert opt.step(g) == 0
+    st = opt.stats(loss_scale=w.loss_scale)
+    s, _ = oracle.sumsq(np.concatenate([x.cpu().numpy().ravel() for x in g]))
+    gn, cc, ap = oracle.clip_coef(s, w.max_norm, w.loss_scale)
+    assert st["global_norm"] == pytest.approx(gn, rel=1e-12)
+    assert st["clip_coef"] == pytest.approx(cc, rel=1e-12)
+    assert st["clipped"] == ap and not st["skipped"] and st["step"] == 1
