@@ -201,3 +201,58 @@ def test_step_fused_argument_errors(lib):
     with pytest.raises(F.Fp8z1Error) as e:
         F.fp8z1_step_fused(L, _hp(), d_grad_params=ptrs.data_ptr() + 4, fp8_shard=t, **common)
     assert e.value.status == F.EALIGN
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_fused_path_with_unaligned_param_views(lib, offset):
+    """Grads and FP8 weights as views that start 1-3 elements into their
+    storage, so every row's misalignment comes from the base address too:
+    the fused norm and step read and write them through the unaligned-row
+    path and must match the aligned, folded path bit for bit."""
+    shapes = [(2, 200, 256), (1, 130, 131), (3, 129, 64)]
+    rng = np.random.default_rng(40 + offset)
+    L = F.fp8z1_build_layout(shapes)
+    nblk = F.fp8z1_layout_info(L)[0]
+    gh = _rows(shapes, rng, 1024e-3)
+    g_store = [torch.zeros(int(np.prod(s)) + 4, device="cuda") for s in shapes]
+    gv = [st[offset:offset + int(np.prod(s))].view(s) for st, s in zip(g_store, shapes)]
+    for v, h in zip(gv, gh):
+        v.copy_(torch.from_numpy(h))
+    c_store = [torch.full((int(np.prod(s)) + 4,), 0xEE, dtype=torch.uint8, device="cuda") for s in shapes]
+    cv = [st[offset:offset + int(np.prod(s))].view(s) for st, s in zip(c_store, shapes)]
+    p = _dev(_rows(shapes, rng, 0.02))
+    ref_g = _dev(gh)  # aligned copies
+    s1 = torch.zeros(1, dtype=torch.float64, device="cuda")
+    f1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s2 = torch.zeros(1, dtype=torch.float64, device="cuda")
+    f2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gf = torch.empty(nblk * B, device="cuda")
+    F.fp8z1_fold_norm(L, F.param_pointers(ref_g), gf, 0, nblk, s1, f1)
+    F.fp8z1_fold_norm(L, F.param_pointers(gv), None, 0, nblk, s2, f2)
+    torch.cuda.synchronize()
+    assert s1.item() == s2.item() and f1.item() == f2.item() == 0
+
+    def state():
+        buf = torch.empty(nblk * B, device="cuda")
+        F.fp8z1_fold(L, F.param_pointers(p), buf, 4, 0, nblk)
+        return buf, torch.zeros(nblk * B, device="cuda"), torch.zeros(nblk * B, device="cuda")
+
+    rp, rm, rv = state()
+    rq = torch.empty(nblk * B, dtype=torch.uint8, device="cuda")
+    rs = torch.empty(nblk, device="cuda")
+    F.fp8z1_step(L, _hp(), gf, rp, rm, rv, rq, rs, 0, nblk, s1, f1)
+    r8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in shapes]
+    F.fp8z1_unfold(L, rq, F.param_pointers(r8), 1, 0, nblk)
+    fp, fm, fv = state()
+    fs = torch.empty(nblk, device="cuda")
+    F.fp8z1_step_fused(L, _hp(), d_grad_params=F.param_pointers(gv), master_shard=fp, m_shard=fm,
+                       v_shard=fv, d_fp8_params=F.param_pointers(cv), scale_shard=fs, b0=0, b1=nblk,
+                       d_sumsq=s2, d_found_inf=f2)
+    torch.cuda.synchronize()
+    for a, b in [(rp, fp), (rm, fm), (rv, fv), (rs, fs)]:
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    for a, b, st, s in zip(r8, cv, c_store, shapes):
+        assert torch.equal(a, b)
+        n = int(np.prod(s))
+        assert (st[:offset] == 0xEE).all() and (st[offset + n:] == 0xEE).all()  # nothing outside the view
+    assert F.fp8z1_device_status(L) == 0

@@ -5,7 +5,6 @@ reproduces every bit."""
 import io
 
 import numpy as np
-
 import pytest
 import torch
 
