@@ -19,6 +19,7 @@ dp_size > 1 the other ranks' norm partials come through ``norm_hook``.
 """
 from __future__ import annotations
 
+from collections import OrderedDict
 from typing import Callable, List, Optional, Sequence
 
 import torch
@@ -52,16 +53,29 @@ class ShardOptimizer:
                        max_norm=max_norm)
         self.scaler = F.fp8z1_loss_scaler(float(loss_scale), 0, 0, int(growth_interval))
         self.norm_hook: Optional[Callable[[torch.Tensor, torch.Tensor], None]] = None
-        self._ptr_cache = {}
+        self._ptr_cache: "OrderedDict[tuple, torch.Tensor]" = OrderedDict()
 
     # -- pointer arrays for fold/unfold ------------------------------------
+    _PTR_CACHE = 16  # distinct tensor sets whose device pointer arrays are kept
+
     def _ptrs(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
-        assert len(tensors) == len(self.shapes)
+        """Device array of the tensors' data pointers (cached per tensor set)."""
+        if len(tensors) != len(self.shapes):
+            raise ValueError(f"expected {len(self.shapes)} tensors, got {len(tensors)}")
+        for t, shp in zip(tensors, self.shapes):
+            if tuple(t.shape) != tuple(shp) and t.numel() != shp[0] * shp[1] * shp[2]:
+                raise ValueError(f"a tensor of shape {tuple(t.shape)} for a param of shape {shp}")
+            if not t.is_contiguous():
+                raise ValueError("param tensors must be contiguous (row-major)")
         key = tuple(t.data_ptr() for t in tensors)
         hit = self._ptr_cache.get(key)
         if hit is None:
             hit = F.param_pointers(tensors, self.device)
             self._ptr_cache[key] = hit
+            if len(self._ptr_cache) > self._PTR_CACHE:
+                self._ptr_cache.popitem(last=False)
+        else:
+            self._ptr_cache.move_to_end(key)
         return hit
 
     def fold_into(self, params: Sequence[torch.Tensor], dst: torch.Tensor, stream=None):
