@@ -428,10 +428,13 @@ def bench_mx(args, rank, world, dist):
 
 
 def _step_source_sha():
+    """Hash of the step kernel's sources: its traffic is stale once they change."""
     import hashlib
-    p = os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", "step.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("step.cu", "update.cuh"):
+        with open(os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 class OracleSample:

@@ -56,7 +56,8 @@ struct StepArgs {
     unsigned* status;
     float* block_cos;            // MON: cosine(master, dequantised) per block
     uint32_t* block_underflow;   // MON: non-zero masters whose code is 0, per block
-    StepScalars c;
+    const StepScalars* dsc;      // DEVSC: the scalars in device memory
+    StepScalars c;               // !DEVSC: the scalars by value
 };
 
 __device__ __forceinline__ float warp_max(float v)
@@ -115,14 +116,18 @@ __device__ __forceinline__ void monitor_add(float p, float dec, float scale, flo
     under += (p != 0.0f && dec == 0.0f) ? 1u : 0u;
 }
 
-template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON>
+template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, bool DEVSC>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
+    __shared__ StepScalars s_c;
     const int tid = threadIdx.x;
-    if (tid == 0) s_gscale = grad_factor(*a.sumsq, a.c);
+    if (tid == 0) {
+        if (DEVSC) s_c = *a.dsc;
+        s_gscale = grad_factor(*a.sumsq, DEVSC ? s_c : a.c);
+    }
 
     // the block's place in its row-major param (only for the row-major forms)
     int rows = 0, cols = 0;
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     }
     __syncthreads();
     const float gs = s_gscale;
+    const StepScalars& c = DEVSC ? s_c : a.c;
 
     const int64_t base = (int64_t)blockIdx.x * (FP8Z1_BLOCK_ELEMS / 4) + tid;
     float pn[4 * kVec];
@@ -177,10 +183,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         float4 p4 = a.master[i];
         float4 m4 = a.mom1[i];
         float4 v4 = a.mom2[i];
-        adamw(gs, a.c, g4.x, p4.x, m4.x, v4.x);
-        adamw(gs, a.c, g4.y, p4.y, m4.y, v4.y);
-        adamw(gs, a.c, g4.z, p4.z, m4.z, v4.z);
-        adamw(gs, a.c, g4.w, p4.w, m4.w, v4.w);
+        adamw(gs, c, g4.x, p4.x, m4.x, v4.x);
+        adamw(gs, c, g4.y, p4.y, m4.y, v4.y);
+        adamw(gs, c, g4.z, p4.z, m4.z, v4.z);
+        adamw(gs, c, g4.w, p4.w, m4.w, v4.w);
         __stcs(a.mom1 + i, m4);
         __stcs(a.mom2 + i, v4);
         __stcs(a.master + i, p4);
@@ -259,11 +265,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     }
 }
 
+// `hp` may be null (scalars in device memory); when given it must be in domain
 int check_common(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* master, const float* m,
                  const float* v, const float* scales, int64_t b0, int64_t b1, const double* d_sumsq,
                  const int32_t* d_found_inf)
 {
-    if (!hp || !master || !m || !v || !scales || !d_sumsq || !d_found_inf || !in_domain(hp))
+    if (!master || !m || !v || !scales || !d_sumsq || !d_found_inf || (hp && !in_domain(hp)))
         return FP8Z1_EINVAL;
     const int st = fp8z1::check_range(L, b0, b1);
     if (st != FP8Z1_OK) return st;
@@ -274,19 +281,20 @@ int check_common(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* m
     return FP8Z1_OK;
 }
 
-template <bool GR, bool CR, bool CF, bool MON>
+template <bool GR, bool CR, bool CF, bool MON, bool DEVSC>
 void launch(const StepArgs& a, int64_t nb, cudaStream_t s)
 {
-    step_kernel<GR, CR, CF, MON><<<(unsigned)nb, kThreads, 0, s>>>(a);
+    step_kernel<GR, CR, CF, MON, DEVSC><<<(unsigned)nb, kThreads, 0, s>>>(a);
 }
 
 template <bool GR, bool CR, bool CF>
 void launch_mon(const StepArgs& a, int64_t nb, cudaStream_t s, bool mon)
 {
+    const bool dev = a.dsc != nullptr;
     if (mon)
-        launch<GR, CR, CF, true>(a, nb, s);
+        dev ? launch<GR, CR, CF, true, true>(a, nb, s) : launch<GR, CR, CF, true, false>(a, nb, s);
     else
-        launch<GR, CR, CF, false>(a, nb, s);
+        dev ? launch<GR, CR, CF, false, true>(a, nb, s) : launch<GR, CR, CF, false, false>(a, nb, s);
 }
 
 }  // namespace
@@ -297,6 +305,7 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
                           const int32_t* d_found_inf, void* stream)
 {
     fp8z1::NvtxRange nvtx_range("fp8z1_step");
+    if (!hp) return FP8Z1_EINVAL;
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
     if (st != FP8Z1_OK) return st;
     if (!grad_shard || !fp8_shard) return FP8Z1_EINVAL;
@@ -315,20 +324,24 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
     a.b0 = b0;
     a.status = L->d_status;
     a.c = scalars(hp);
-    launch<false, false, true, false>(a, b1 - b0, static_cast<cudaStream_t>(stream));
+    launch<false, false, true, false, false>(a, b1 - b0, static_cast<cudaStream_t>(stream));
     return fp8z1::launch_status();
 }
 
-extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
-                                const float* const* d_grad_params, float* master_shard, float* m_shard,
-                                float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
-                                float* scale_shard, float* block_cos, uint32_t* block_underflow,
-                                int64_t b0, int64_t b1, const double* d_sumsq,
-                                const int32_t* d_found_inf, void* stream)
+namespace {
+
+int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const StepScalars* h_scalars,
+                    StepScalars* d_scalars,
+                    const float* grad_shard, const float* const* d_grad_params, float* master_shard,
+                    float* m_shard, float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
+                    float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0, int64_t b1,
+                    const double* d_sumsq, const int32_t* d_found_inf, void* stream)
 {
-    fp8z1::NvtxRange nvtx_range("fp8z1_step_fused");
+    // exactly one scalar source: hp by value, or d_scalars
+    if ((hp == nullptr) == (d_scalars == nullptr)) return FP8Z1_EINVAL;
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
     if (st != FP8Z1_OK) return st;
+    if (d_scalars && !fp8z1::aligned(d_scalars, 4)) return FP8Z1_EALIGN;
     // exactly one grad source, at least one code destination
     if ((grad_shard == nullptr) == (d_grad_params == nullptr)) return FP8Z1_EINVAL;
     if (fp8_shard == nullptr && d_fp8_params == nullptr) return FP8Z1_EINVAL;
@@ -356,9 +369,15 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
     a.block_cos = block_cos;
     a.block_underflow = block_underflow;
     a.status = L->d_status;
-    a.c = scalars(hp);
+    a.dsc = d_scalars;
+    if (hp) a.c = scalars(hp);
     const int64_t nb = b1 - b0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (h_scalars && cudaMemcpyAsync(d_scalars, h_scalars, sizeof(StepScalars),
+                                     cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
     const bool gr = d_grad_params != nullptr, cr = d_fp8_params != nullptr, cf = fp8_shard != nullptr;
     const bool mon = block_cos != nullptr;
     if (gr) {
@@ -371,4 +390,41 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
         else launch_mon<false, false, true>(a, nb, s, mon);
     }
     return fp8z1::launch_status();
+}
+
+}  // namespace
+
+extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                                const float* const* d_grad_params, float* master_shard, float* m_shard,
+                                float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
+                                float* scale_shard, float* block_cos, uint32_t* block_underflow,
+                                int64_t b0, int64_t b1, const double* d_sumsq,
+                                const int32_t* d_found_inf, void* stream)
+{
+    fp8z1::NvtxRange nvtx_range("fp8z1_step_fused");
+    if (!hp) return FP8Z1_EINVAL;
+    return step_fused_impl(L, hp, nullptr, nullptr, grad_shard, d_grad_params, master_shard, m_shard, v_shard,
+                           fp8_shard, d_fp8_params, scale_shard, block_cos, block_underflow, b0, b1, d_sumsq,
+                           d_found_inf, stream);
+}
+
+extern "C" int fp8z1_step_fused_dev(const fp8z1_layout* L, const fp8z1_step_scalars* h_scalars,
+                                    fp8z1_step_scalars* d_scalars, const float* grad_shard,
+                                    const float* const* d_grad_params, float* master_shard, float* m_shard,
+                                    float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
+                                    float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0,
+                                    int64_t b1, const double* d_sumsq, const int32_t* d_found_inf, void* stream)
+{
+    fp8z1::NvtxRange nvtx_range("fp8z1_step_fused_dev");
+    if (!d_scalars) return FP8Z1_EINVAL;
+    return step_fused_impl(L, nullptr, h_scalars, d_scalars, grad_shard, d_grad_params, master_shard, m_shard,
+                           v_shard, fp8_shard, d_fp8_params, scale_shard, block_cos, block_underflow, b0, b1,
+                           d_sumsq, d_found_inf, stream);
+}
+
+extern "C" int fp8z1_step_scalars_from_hp(const fp8z1_adamw_hp* hp, fp8z1_step_scalars* out)
+{
+    if (!hp || !out || !in_domain(hp)) return FP8Z1_EINVAL;
+    *out = scalars(hp);
+    return FP8Z1_OK;
 }

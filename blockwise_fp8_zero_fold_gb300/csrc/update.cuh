@@ -21,9 +21,7 @@
 
 namespace fp8z1 {
 
-struct StepScalars {
-    float beta1, beta2, omb1, omb2, eps, step_size, inv_sqrt_bc2, decay, max_norm, loss_scale;
-};
+using StepScalars = fp8z1_step_scalars;
 
 // The unscale and clip folded into one factor, from the global sum of squares
 // of the loss-scaled grads (formed in double, as the host would).

@@ -51,6 +51,11 @@ class fp8z1_adamw_hp(C.Structure):
                 ("loss_scale", C.c_float), ("step", C.c_int64)]
 
 
+class fp8z1_step_scalars(C.Structure):
+    _fields_ = [(n, C.c_float) for n in ("beta1", "beta2", "omb1", "omb2", "eps", "step_size",
+                                          "inv_sqrt_bc2", "decay", "max_norm", "loss_scale")]
+
+
 class fp8z1_loss_scaler(C.Structure):
     _fields_ = [("scale", C.c_float), ("step", C.c_int64), ("good_steps", C.c_int32),
                 ("growth_interval", C.c_int32)]
@@ -81,6 +86,9 @@ _SIGS = {
     "fp8z1_fold_norm": (C.c_int, [_P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_step_fused": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, _P, _P,
                                    _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_step_fused_dev": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                       C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_step_scalars_from_hp": (C.c_int, [C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_step_scalars)]),
     "fp8z1_paramwise_split": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, _P, _P,
                                         C.POINTER(C.c_int64)]),
     "fp8z1_mx_build_layout": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, C.c_uint32,
@@ -281,6 +289,32 @@ def fp8z1_step_fused(layout: Layout, hp: fp8z1_adamw_hp, *, grad_shard=None, d_g
                                   _ptr(block_underflow), int(b0), int(b1),
                                   _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_step_fused")
+
+
+def fp8z1_step_fused_dev(layout: Layout, h_scalars, d_scalars, *, grad_shard=None, d_grad_params=None,
+                         master_shard, m_shard, v_shard, fp8_shard=None, d_fp8_params=None,
+                         scale_shard, block_cos=None, block_underflow=None, b0: int, b1: int, d_sumsq,
+                         d_found_inf, stream=None):
+    """fp8z1_step_fused with the per-step scalars read from device memory
+    ``d_scalars`` (40 bytes), after a copy from ``h_scalars`` (page-locked
+    host memory, or None for no copy) enqueued on the same stream."""
+    _check(lib().fp8z1_step_fused_dev(layout.handle, _ptr(h_scalars), _ptr(d_scalars), _ptr(grad_shard),
+                                      _ptr(d_grad_params), _ptr(master_shard), _ptr(m_shard), _ptr(v_shard),
+                                      _ptr(fp8_shard), _ptr(d_fp8_params), _ptr(scale_shard),
+                                      _ptr(block_cos), _ptr(block_underflow), int(b0), int(b1),
+                                      _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_step_fused_dev")
+
+
+def fp8z1_step_scalars_from_hp(hp: fp8z1_adamw_hp, out=None) -> fp8z1_step_scalars:
+    """The FP32 scalars of one step (host).  ``out``: a tensor or address of
+    40 bytes to fill in place (pinned host memory, say); the struct is
+    returned either way."""
+    sc = fp8z1_step_scalars()
+    _check(lib().fp8z1_step_scalars_from_hp(C.byref(hp), C.byref(sc)), "fp8z1_step_scalars_from_hp")
+    if out is not None:
+        C.memmove(_ptr(out), C.addressof(sc), C.sizeof(sc))
+    return sc
 
 
 def fp8z1_paramwise_split(shapes, dp_size: int):

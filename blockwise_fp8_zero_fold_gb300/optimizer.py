@@ -19,6 +19,7 @@ dp_size > 1 the other ranks' norm partials come through ``norm_hook``.
 """
 from __future__ import annotations
 
+import ctypes as C
 from collections import OrderedDict
 from typing import Callable, List, Optional, Sequence
 
@@ -258,6 +259,12 @@ class ShardOptimizer:
         self.launch_step(grads, fp8_params, stream)
         return self.finish_step()
 
+    def capture(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]] = None,
+                pool=None, slots: int = 2) -> "CapturedStep":
+        """Capture one fused step over these grad (and FP8 weight) tensors in a
+        CUDA graph; see ``CapturedStep``."""
+        return CapturedStep(self, grads, fp8_params, pool, slots)
+
     def stats(self, loss_scale: Optional[float] = None) -> dict:
         """Numbers for logging the last step (reads two device scalars): the
         global grad norm and clip coefficient (on this shard's sum of squares,
@@ -269,6 +276,94 @@ class ShardOptimizer:
         norm, coef = (float("nan"), float("nan")) if found else F.fp8z1_clip_coef(s, self.hp["max_norm"], used)
         return {"global_norm": norm, "clip_coef": coef, "clipped": bool(not found and coef < 1.0),
                 "skipped": bool(found), "loss_scale": self.scaler.scale, "step": self.scaler.step}
+
+
+class CapturedStep:
+    """One fused step of a ``ShardOptimizer`` as a CUDA graph: zero the norm
+    accumulators, the norm read from the row-major grads (then the norm hook,
+    which is captured too, so it must be capturable: an NCCL all-reduce is),
+    a copy of the step's scalars from page-locked host memory, and the step
+    reading them from device memory (fp8z1_step_fused_dev).  A replay thus
+    costs one graph launch however many entry points the step has.
+
+    The graph holds the addresses of the tensors it was captured with: each
+    step, write the new grads into those same ``grads`` tensors, and read the
+    FP8 weights from those ``fp8_params`` (or ``codes`` when None).  t and S
+    live on the host as before: ``replay`` writes this step's scalars to the
+    pinned slot its graph copies from; ``step`` also reads found_inf and
+    updates the loss scaler, like ``ShardOptimizer.step``.  The step is
+    captured ``slots`` times, each graph copying from its own pinned slot and
+    replayed in turn, so the host can enqueue step k+1 before step k's copy of
+    its scalars has run."""
+
+    def __init__(self, opt: "ShardOptimizer", grads, fp8_params=None, pool=None, slots: int = 2):
+        if not opt.fused:
+            raise ValueError("a captured step runs the fused path")
+        self.opt = opt
+        self.grads = list(grads)
+        self.fp8_params = None if fp8_params is None else list(fp8_params)
+        # the graph reads these pointer arrays: keep them alive with it
+        self._gptrs = opt._ptrs(self.grads)
+        self._fptrs = None if fp8_params is None else opt._ptrs(self.fp8_params)
+        nsc = C.sizeof(F.fp8z1_step_scalars) // 4
+        self._h = [torch.zeros(nsc, dtype=torch.float32, pin_memory=True) for _ in range(slots)]
+        self._d = torch.zeros(nsc, dtype=torch.float32, device=opt.device)
+        self._hp_struct = F.make_hp(step=1, loss_scale=1.0, **opt.hp)
+        self._done = [torch.cuda.Event() for _ in range(slots)]
+        self._next = 0
+        # load every kernel once outside the capture: found_inf preset makes
+        # the step a no-op, and the accumulators are zeroed in the graph
+        side = torch.cuda.Stream(opt.device)
+        side.wait_stream(torch.cuda.current_stream(opt.device))
+        with torch.cuda.stream(side):
+            self._write(self._h[0])
+            opt.found_inf.fill_(1)
+            self._enqueue(self._h[0], norm_hook=False)
+            opt.sumsq.zero_()
+            opt.found_inf.zero_()
+        side.synchronize()
+        torch.cuda.current_stream(opt.device).wait_stream(side)
+        self.graphs = []
+        for h in self._h:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, pool=pool, stream=side):  # nothing is allocated inside
+                opt.sumsq.zero_()
+                opt.found_inf.zero_()
+                self._enqueue(h, norm_hook=True)
+            self.graphs.append(g)
+
+    def _write(self, h: torch.Tensor):
+        o, hp = self.opt, self._hp_struct
+        hp.step = o.scaler.step + 1
+        hp.loss_scale = o.scaler.scale
+        F.fp8z1_step_scalars_from_hp(hp, h)
+
+    def _enqueue(self, h, norm_hook: bool):
+        o = self.opt
+        F.fp8z1_fold_norm(o.layout, self._gptrs, None, o.b0, o.b1, o.sumsq, o.found_inf)
+        if norm_hook and o.norm_hook is not None:
+            o.norm_hook(o.sumsq, o.found_inf)
+        F.fp8z1_step_fused_dev(o.layout, h, self._d, d_grad_params=self._gptrs,
+                               master_shard=o.master, m_shard=o.m, v_shard=o.v,
+                               fp8_shard=o.codes if self._fptrs is None else None, d_fp8_params=self._fptrs,
+                               scale_shard=o.scales, b0=o.b0, b1=o.b1, d_sumsq=o.sumsq,
+                               d_found_inf=o.found_inf)
+
+    def replay(self):
+        """Enqueue one step on the current stream (no host synchronisation,
+        unless this slot's previous replay has not finished).  t and S are
+        the scaler's when the step is enqueued: ``finish_step`` between
+        replays advances them, as with ``ShardOptimizer.launch_step``."""
+        k = self._next
+        self._next = (k + 1) % len(self.graphs)
+        self._done[k].synchronize()  # its pinned scalars are about to be overwritten
+        self._write(self._h[k])
+        self.graphs[k].replay()
+        self._done[k].record()
+
+    def step(self) -> int:
+        self.replay()
+        return self.opt.finish_step()
 
 
 class MxShardOptimizer:

@@ -270,6 +270,37 @@ int fp8z1_step_fused(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const
                      float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0,
                      int64_t b1, const double* d_sumsq, const int32_t* d_found_inf, void* stream);
 
+/* ---- the step with its scalars in device memory (for CUDA graphs) --------- */
+
+/* The FP32 scalars one step uses, derived on the host in double from
+ * fp8z1_adamw_hp and rounded once: beta1, beta2, 1 - beta1, 1 - beta2, eps,
+ * lr / (1 - beta1^t), 1 / sqrt(1 - beta2^t), 1 - lr * wd, max_norm, S. */
+typedef struct {
+    float beta1, beta2, omb1, omb2, eps, step_size, inv_sqrt_bc2, decay, max_norm, loss_scale;
+} fp8z1_step_scalars;
+
+/* Fill *out from *hp (host only; EINVAL when hp is out of its domain). */
+int fp8z1_step_scalars_from_hp(const fp8z1_adamw_hp* hp, fp8z1_step_scalars* out);
+
+/* fp8z1_step_fused with the per-step scalars read from DEVICE memory
+ * (`d_scalars`, 4-byte aligned) when the kernel runs, instead of passed by
+ * value at launch.  When `h_scalars` is not NULL, the call first enqueues on
+ * `stream` a copy of *h_scalars into *d_scalars.  Under CUDA stream capture
+ * that copy becomes a graph node which reads *h_scalars at every replay.
+ * `h_scalars` must then be page-locked host memory (cudaHostAlloc or
+ * cudaHostRegister), and the caller writes the next step's scalars there
+ * (fp8z1_step_scalars_from_hp) before each replay, once the previous replay's
+ * copy has run.  t and S change every step, so this is what lets a captured
+ * step replay correctly.  The scalars are not checked on the device.  Every
+ * result is that of fp8z1_step_fused with the hp they were made from.
+ * Errors: as fp8z1_step_fused; ECUDA when the copy cannot be enqueued. */
+int fp8z1_step_fused_dev(const fp8z1_layout* layout, const fp8z1_step_scalars* h_scalars,
+                         fp8z1_step_scalars* d_scalars, const float* grad_shard,
+                         const float* const* d_grad_params, float* master_shard, float* m_shard, float* v_shard,
+                         uint8_t* fp8_shard, uint8_t* const* d_fp8_params, float* scale_shard, float* block_cos,
+                         uint32_t* block_underflow, int64_t b0, int64_t b1, const double* d_sumsq,
+                         const int32_t* d_found_inf, void* stream);
+
 /* ---- param-wise split (§参数粒度切分; host only) ---------------------------- */
 
 /* The page's alternative to the block-wise split, for comparing padding

@@ -10,6 +10,10 @@
  *                                  writes master, scales and FP8 weights to
  *                                  <out> (raw: float32 x 6*16384, float32 x 6,
  *                                  uint8 x 300*200)
+ *   c_abi_example graph <in> <out> the same, as three steps (t = 1, 2, 3, the
+ *                                  same grads) replayed from one CUDA graph:
+ *                                  zero the accumulators, norm, copy of the
+ *                                  step scalars from pinned memory, step
  */
 #include <cuda_runtime.h>
 #include <stdio.h>
@@ -67,7 +71,7 @@ static int host_part(void)
     return 0;
 }
 
-static int gpu_part(const char* in, const char* out)
+static int gpu_part(const char* in, const char* out, int graph)
 {
     const int64_t R = 300, C = 200, n_real = R * C, nblk = 6, n = nblk * FP8Z1_BLOCK_ELEMS;
     float* h = (float*)malloc(sizeof(float) * 2 * n_real);
@@ -102,11 +106,42 @@ static int gpu_part(const char* in, const char* out)
     CUDA(cudaMemcpy(d_ptrs, ptrs, sizeof ptrs, cudaMemcpyHostToDevice));
     /* init: fold the row-major master; then one fused step */
     CHECK(fp8z1_fold(L, (const void* const*)&d_ptrs[0], d_master, 4, 0, nblk, NULL));
-    CHECK(fp8z1_fold_norm(L, (const float* const*)&d_ptrs[1], NULL, 0, nblk, d_sumsq, d_found, NULL));
     fp8z1_adamw_hp hp = {1e-3f, 0.9f, 0.95f, 1e-8f, 0.1f, 1.0f, 1024.0f, 1};
-    CHECK(fp8z1_step_fused(L, &hp, NULL, (const float* const*)&d_ptrs[1], d_master, d_m, d_v, NULL,
-                           (uint8_t* const*)&d_ptrs[2], d_scales, NULL, NULL, 0, nblk, d_sumsq, d_found,
-                           NULL));
+    if (!graph) {
+        CHECK(fp8z1_fold_norm(L, (const float* const*)&d_ptrs[1], NULL, 0, nblk, d_sumsq, d_found, NULL));
+        CHECK(fp8z1_step_fused(L, &hp, NULL, (const float* const*)&d_ptrs[1], d_master, d_m, d_v, NULL,
+                               (uint8_t* const*)&d_ptrs[2], d_scales, NULL, NULL, 0, nblk, d_sumsq, d_found,
+                               NULL));
+    } else {
+        fp8z1_step_scalars *h_sc, *d_sc;
+        cudaStream_t st;
+        cudaGraph_t g;
+        cudaGraphExec_t ge;
+        CUDA(cudaHostAlloc((void**)&h_sc, sizeof *h_sc, cudaHostAllocDefault));
+        CUDA(cudaMalloc((void**)&d_sc, sizeof *d_sc));
+        CUDA(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+        CHECK(fp8z1_step_scalars_from_hp(&hp, h_sc));
+        CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+        CUDA(cudaMemsetAsync(d_sumsq, 0, sizeof(double), st));
+        CUDA(cudaMemsetAsync(d_found, 0, sizeof(int32_t), st));
+        CHECK(fp8z1_fold_norm(L, (const float* const*)&d_ptrs[1], NULL, 0, nblk, d_sumsq, d_found, st));
+        CHECK(fp8z1_step_fused_dev(L, h_sc, d_sc, NULL, (const float* const*)&d_ptrs[1], d_master, d_m, d_v,
+                                   NULL, (uint8_t* const*)&d_ptrs[2], d_scales, NULL, NULL, 0, nblk, d_sumsq,
+                                   d_found, st));
+        CUDA(cudaStreamEndCapture(st, &g));
+        CUDA(cudaGraphInstantiate(&ge, g, 0));
+        for (int64_t t = 1; t <= 3; ++t) {
+            hp.step = t;
+            CHECK(fp8z1_step_scalars_from_hp(&hp, h_sc)); /* the previous replay has finished */
+            CUDA(cudaGraphLaunch(ge, st));
+            CUDA(cudaStreamSynchronize(st));
+        }
+        CUDA(cudaGraphExecDestroy(ge));
+        CUDA(cudaGraphDestroy(g));
+        CUDA(cudaStreamDestroy(st));
+        CUDA(cudaFree(d_sc));
+        CUDA(cudaFreeHost(h_sc));
+    }
     CUDA(cudaDeviceSynchronize());
     float* hm = (float*)malloc(sizeof(float) * n);
     float hs[6];
@@ -128,7 +163,8 @@ static int gpu_part(const char* in, const char* out)
 int main(int argc, char** argv)
 {
     if (argc >= 2 && strcmp(argv[1], "host") == 0) return host_part();
-    if (argc >= 4 && strcmp(argv[1], "gpu") == 0) return gpu_part(argv[2], argv[3]);
-    fprintf(stderr, "usage: %s host | gpu <in> <out>\n", argv[0]);
+    if (argc >= 4 && strcmp(argv[1], "gpu") == 0) return gpu_part(argv[2], argv[3], 0);
+    if (argc >= 4 && strcmp(argv[1], "graph") == 0) return gpu_part(argv[2], argv[3], 1);
+    fprintf(stderr, "usage: %s host | gpu <in> <out> | graph <in> <out>\n", argv[0]);
     return 2;
 }

@@ -50,13 +50,16 @@ def test_host_calls_from_c(exe):
 
 
 @pytest.mark.gpu
-def test_one_step_from_c(exe, tmp_path):
+@pytest.mark.parametrize("mode,steps", [("gpu", 1), ("graph", 3)])
+def test_steps_from_c(exe, tmp_path, mode, steps):
+    """One step, or three replays of one captured graph (t = 1, 2, 3 written
+    to pinned memory between them), from plain C against the oracle."""
     rng = np.random.default_rng(31)
     g = (rng.standard_normal((300, 200)) * 1024e-3).astype(np.float32)
     p = (rng.standard_normal((300, 200)) * 0.02).astype(np.float32)
     fin, fout = tmp_path / "in.bin", tmp_path / "out.bin"
     np.concatenate([g.ravel(), p.ravel()]).tofile(fin)
-    r = subprocess.run([exe, "gpu", str(fin), str(fout)], capture_output=True, text=True)
+    r = subprocess.run([exe, mode, str(fin), str(fout)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     raw = np.fromfile(fout, dtype=np.uint8)
     n = 6 * 16384
@@ -66,8 +69,9 @@ def test_one_step_from_c(exe, tmp_path):
     shapes = [(1, 300, 200)]
     og, op = oracle.fold(shapes, [g[None]]), oracle.fold(shapes, [p[None]])
     s, f = oracle.sumsq(og)
-    q, sc, _ = oracle.step(oracle.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1024.0, 1), s, f, og, op,
-                           np.zeros_like(op), np.zeros_like(op))
+    om, ov = np.zeros_like(op), np.zeros_like(op)
+    for t in range(1, steps + 1):
+        q, sc, _ = oracle.step(oracle.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 1024.0, t), s, f, og, op, om, ov)
     want = np.zeros((1, 300, 200), np.uint8)
     oracle.unfold(shapes, q, [want])
     assert np.array_equal(master.view(np.uint32), op.view(np.uint32))

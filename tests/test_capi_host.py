@@ -119,6 +119,11 @@ def test_argument_errors_enqueue_nothing():
                   F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 0.0, 1),
                   F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 0.0, 1024.0, 1)]:
         assert lib.fp8z1_step(L.handle, C.byref(badhp), p, p, p, p, p, p, 0, 3, p, p, None) == F.EINVAL
+    d = np.zeros(16, np.float32).ctypes.data
+    assert lib.fp8z1_step_fused_dev(L.handle, None, None, None, p, p, p, p, p, None, p, None, None, 0, 3, p, p,
+                                    None) == F.EINVAL
+    assert lib.fp8z1_step_fused_dev(L.handle, None, d, None, p, p, p, p, p, None, p, None, None, 0, 3, p, p,
+                                    None) == F.ENODEV
     assert lib.fp8z1_device_status(L.handle, C.byref(C.c_uint32())) == F.ENODEV
     assert F.fp8z1_strerror(F.EALIGN) == "misaligned pointer"
     with pytest.raises(F.Fp8z1Error):
@@ -190,3 +195,23 @@ def test_clip_coef_host_matches_oracle_and_golden(row):
     assert (c < 1.0) == bool(int(applies))
     with pytest.raises(F.Fp8z1Error):
         F.fp8z1_clip_coef(-1.0, 1.0, 1.0)
+
+
+def test_step_scalars_from_hp():
+    """The per-step FP32 scalars: each formed in double and rounded once."""
+    lr, b1, b2, eps, wd, mx, ls, t = 3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, 4096.0, 7
+    hp = F.make_hp(lr, b1, b2, eps, wd, mx, ls, t)
+    sc = F.fp8z1_step_scalars_from_hp(hp)
+    f32 = lambda x: float(np.float32(x))  # noqa: E731
+    lr, b1, b2, eps, wd = (f32(x) for x in (lr, b1, b2, eps, wd))
+    want = dict(beta1=b1, beta2=b2, omb1=f32(1 - b1), omb2=f32(1 - b2), eps=eps,
+                step_size=f32(lr / (1 - b1 ** t)), inv_sqrt_bc2=f32(1 / np.sqrt(1 - b2 ** t)),
+                decay=f32(1 - lr * wd), max_norm=mx, loss_scale=ls)
+    for k, v in want.items():
+        assert getattr(sc, k) == v, k
+    out = np.zeros(10, np.float32)
+    F.fp8z1_step_scalars_from_hp(hp, out)
+    assert out[5] == want["step_size"] and out[9] == ls
+    with pytest.raises(F.Fp8z1Error) as e:
+        F.fp8z1_step_scalars_from_hp(F.make_hp(lr, b1, b2, eps, wd, mx, ls, 0))
+    assert e.value.status == F.EINVAL
