@@ -274,21 +274,29 @@ def bench_ours(args, rank, world, dist):
         h2d = sum(h.numel() * 4 for h in hgrads)
         d2h = sum(h.numel() for h in hfp8) + nblk * 4 + 4
 
-        def e2e_step():
+        def e2e_step(wait):
             # the public API's host path: chunked copies overlapped with the norm
-            # and the update (ShardOptimizer.step_from_host)
-            opt.step_from_host(hgrads, hfp8, hscales, grads=grads, fp8_params=fp8)
+            # and the update (ShardOptimizer.step_from_host); without waiting,
+            # the next step's grads go in while this step's FP8 weights come out
+            return opt.step_from_host(hgrads, hfp8, hscales, grads=grads, fp8_params=fp8, wait=wait)
 
-        e2e_step()
+        e2e_step(True)
         if dist is not None:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            e2e_step()
+            e2e_step(True)
+        wall_sync = max_over_ranks(time.perf_counter() - t0, dist, dev)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step(False)
+        opt.finish_host_step()
         wall = max_over_ranks(time.perf_counter() - t0, dist, dev)
         e2e = {"value": whole_job_rate(n_pad, world, args.e2e_steps, wall), "unit": "elem/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": wall / args.e2e_steps * 1e3, "steps": args.e2e_steps}
+               "ms_per_step": wall / args.e2e_steps * 1e3, "steps": args.e2e_steps,
+               "mode": "steps enqueued back to back (step_from_host wait=False), then finish_host_step",
+               "ms_per_step_one_at_a_time": wall_sync / args.e2e_steps * 1e3}
         del hgrads, hfp8
 
     out = {
@@ -528,7 +536,7 @@ def main():
     ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=1)
     args = ap.parse_args()

@@ -55,6 +55,8 @@ class ShardOptimizer:
         self.scaler = F.fp8z1_loss_scaler(float(loss_scale), 0, 0, int(growth_interval))
         self.norm_hook: Optional[Callable[[torch.Tensor, torch.Tensor], None]] = None
         self._ptr_cache: "OrderedDict[tuple, torch.Tensor]" = OrderedDict()
+        self._host_pending: Optional[int] = None  # step_from_host(wait=False) in flight
+        self._host_slot = 0
 
     # -- pointer arrays for fold/unfold ------------------------------------
     _PTR_CACHE = 16  # distinct tensor sets whose device pointer arrays are kept
@@ -112,6 +114,7 @@ class ShardOptimizer:
         """Everything a resumed run needs: the shard's folded FP32 master / m /
         v, the codes and scales, and the host scalars (t, S, clean-step count).
         The buffers are the 1-D block layout itself, so a reload is a copy."""
+        self.finish_host_step()
         return {
             "shapes": [tuple(s) for s in self.shapes], "b0": self.b0, "b1": self.b1,
             "master": self.master.cpu(), "m": self.m.cpu(), "v": self.v.cpu(),
@@ -122,6 +125,7 @@ class ShardOptimizer:
         }
 
     def load_state_dict(self, sd: dict):
+        self.finish_host_step()
         if [tuple(s) for s in sd["shapes"]] != [tuple(s) for s in self.shapes] or \
                 (sd["b0"], sd["b1"]) != (self.b0, self.b1):
             raise ValueError("checkpoint was taken for another layout or shard")
@@ -136,6 +140,8 @@ class ShardOptimizer:
     def launch_step(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
                     stream=None):
         """Enqueue one step (no host synchronisation)."""
+        if self._host_pending is not None:
+            raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
         self.sumsq.zero_()
         self.found_inf.zero_()
         hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
@@ -185,7 +191,8 @@ class ShardOptimizer:
 
     def step_from_host(self, host_grads: Sequence[torch.Tensor], host_fp8: Sequence[torch.Tensor],
                        host_scales: Optional[torch.Tensor] = None, grads: Optional[Sequence[torch.Tensor]] = None,
-                       fp8_params: Optional[Sequence[torch.Tensor]] = None, target_blocks: int = 1792) -> int:
+                       fp8_params: Optional[Sequence[torch.Tensor]] = None, target_blocks: int = 1792,
+                       wait: bool = True) -> Optional[int]:
         """One step whose grads arrive from (pinned) host memory and whose FP8
         weights (and scales) go back to it, with the copies overlapped: chunk
         c's grads are copied on a copy stream while chunk c-1's norm runs, and
@@ -194,7 +201,16 @@ class ShardOptimizer:
         (allocated on first use when not given).  Fused path, whole-buffer
         shards only: the copies move whole rows, and a shard that starts or
         ends inside a row of blocks would copy back rows it did not update.
-        Host tensors should be pinned for the copies to overlap."""
+        Host tensors should be pinned for the copies to overlap.
+
+        ``wait=False`` returns None once the step is enqueued, so that the
+        next call's grads go in while this step's update runs and its FP8
+        weights come out.  A chunk's grads then wait only for this step's
+        update of that chunk, and its update waits only for this step's copy
+        of that chunk's FP8 weights.  The step's found_inf is read when the next
+        call needs t and S (the norm has long finished by then), or by
+        ``finish_host_step``, which also waits for the copies back: the host
+        FP8 weights and scales are complete only after it."""
         assert self.fused, "step_from_host runs the fused path"
         if (self.b0, self.b1) != (0, self.nblk):
             raise ValueError("step_from_host needs the whole buffer as the shard (dp_size 1)")
@@ -207,46 +223,78 @@ class ShardOptimizer:
                                                              for s in self.shapes]
             self._dev_fp8 = fp8_params
         if getattr(self, "_chunks_cache", None) is None or self._chunks_cache[0] != target_blocks:
-            self._chunks_cache = (target_blocks, self._host_chunks(target_blocks))
+            if self._host_pending is not None:
+                self.finish_host_step()
+            chunks = self._host_chunks(target_blocks)
+            self._chunks_cache = (target_blocks, chunks)
             self._copy_in = torch.cuda.Stream(self.device)
             self._copy_out = torch.cuda.Stream(self.device)
-            self._flag = torch.empty(1, dtype=torch.int32, pin_memory=True)
+            self._flags = [torch.zeros(1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+            self._norm_done = [torch.cuda.Event() for _ in range(2)]
+            self._h2d_done = [torch.cuda.Event() for _ in chunks]
+            self._upd_done = [torch.cuda.Event() for _ in chunks]
+            self._d2h_done = [torch.cuda.Event() for _ in chunks]
+            self._scales_done = torch.cuda.Event()
         chunks = self._chunks_cache[1]
+        prev = self._host_pending  # the step still in flight, if any
         comp = torch.cuda.current_stream(self.device)
         gptrs, fptrs = self._ptrs(grads), self._ptrs(fp8_params)
-        self.sumsq.zero_()
+        self.sumsq.zero_()  # after the previous step's update on this stream
         self.found_inf.zero_()
-        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
-        ready = []
-        for p, e, r0, r1, k0, k1 in chunks:  # grads in, norm as each chunk lands
-            ev = torch.cuda.Event()
+        for c, (p, e, r0, r1, k0, k1) in enumerate(chunks):  # grads in, norm as each chunk lands
             with torch.cuda.stream(self._copy_in):
+                if prev is not None:
+                    self._copy_in.wait_event(self._upd_done[c])
                 grads[p][e, r0:r1].copy_(host_grads[p][e, r0:r1], non_blocking=True)
-                ev.record(self._copy_in)
-            comp.wait_event(ev)
+                self._h2d_done[c].record(self._copy_in)
+            comp.wait_event(self._h2d_done[c])
             F.fp8z1_fold_norm(self.layout, gptrs, None, k0, k1, self.sumsq, self.found_inf, comp)
         if self.norm_hook is not None:
             self.norm_hook(self.sumsq, self.found_inf)
-        for p, e, r0, r1, k0, k1 in chunks:  # update, FP8 weights out as each chunk is done
-            F.fp8z1_step_fused(self.layout, hp, d_grad_params=gptrs, master_shard=self.master[(k0 - self.b0) * F.BLOCK_ELEMS:],
-                               m_shard=self.m[(k0 - self.b0) * F.BLOCK_ELEMS:], v_shard=self.v[(k0 - self.b0) * F.BLOCK_ELEMS:],
-                               d_fp8_params=fptrs, scale_shard=self.scales[k0 - self.b0:], b0=k0, b1=k1,
-                               d_sumsq=self.sumsq, d_found_inf=self.found_inf, stream=comp)
-            ev = torch.cuda.Event()
-            ev.record(comp)
-            self._copy_out.wait_event(ev)
+        slot = self._host_slot
+        self._host_slot ^= 1
+        self._flags[slot].copy_(self.found_inf, non_blocking=True)
+        self._norm_done[slot].record(comp)
+        if prev is not None:  # t and S of this step follow the previous step's found_inf
+            self._retire_host_step(prev)
+        hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
+        if prev is not None:
+            comp.wait_event(self._scales_done)
+        for c, (p, e, r0, r1, k0, k1) in enumerate(chunks):  # update, FP8 weights out as each chunk is done
+            if prev is not None:
+                comp.wait_event(self._d2h_done[c])
+            o = (k0 - self.b0) * F.BLOCK_ELEMS
+            F.fp8z1_step_fused(self.layout, hp, d_grad_params=gptrs, master_shard=self.master[o:],
+                               m_shard=self.m[o:], v_shard=self.v[o:], d_fp8_params=fptrs,
+                               scale_shard=self.scales[k0 - self.b0:], b0=k0, b1=k1, d_sumsq=self.sumsq,
+                               d_found_inf=self.found_inf, stream=comp)
+            self._upd_done[c].record(comp)
+            self._copy_out.wait_event(self._upd_done[c])
             with torch.cuda.stream(self._copy_out):
                 host_fp8[p][e, r0:r1].copy_(fp8_params[p][e, r0:r1], non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(comp)
-        self._copy_out.wait_event(ev)
+                self._d2h_done[c].record(self._copy_out)
         with torch.cuda.stream(self._copy_out):
             if host_scales is not None:
                 host_scales.copy_(self.scales, non_blocking=True)
-            self._flag.copy_(self.found_inf, non_blocking=True)
-        self._copy_out.synchronize()
-        found = int(self._flag.item())
+            self._scales_done.record(self._copy_out)
+        self._host_pending = slot
+        return self.finish_host_step() if wait else None
+
+    def _retire_host_step(self, slot: int) -> int:
+        self._norm_done[slot].synchronize()
+        found = int(self._flags[slot].item())
         F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
+    def finish_host_step(self) -> Optional[int]:
+        """Wait for the last ``step_from_host`` to finish, its FP8 weights and
+        scales to reach the host, and return its found_inf (None when no step
+        is in flight)."""
+        if self._host_pending is None:
+            return None
+        self._copy_out.synchronize()
+        found = self._retire_host_step(self._host_pending)
+        self._host_pending = None
         return found
 
     def finish_step(self) -> int:
@@ -270,6 +318,7 @@ class ShardOptimizer:
         global grad norm and clip coefficient (on this shard's sum of squares,
         after any norm hook), the loss scale the step used (pass it when the
         scaler has moved since), t and S now, and whether it was skipped."""
+        self.finish_host_step()
         s = float(self.sumsq.item())
         found = int(self.found_inf.item())
         used = self.scaler.scale if loss_scale is None else loss_scale

@@ -94,6 +94,42 @@ def test_step_from_host_matches_device_path(lib, max_norm):
         _make(synth.workload("tiny"), 0).step_from_host([], [])
 
 
+def test_pipelined_steps_from_host(lib):
+    """Four steps from host buffers enqueued back to back (wait=False: step
+    k+1's grads go in while step k's update and copies back run), the third
+    skipped for a nan: the same state, FP8 weights, scales and loss scaler
+    as the device-resident path stepping one at a time."""
+    w = synth.workload("tiny", shapes=[(3, 512, 384), (1, 1000, 131), (2, 130, 260)], dp=1, rank=0,
+                       m_sigma=1e-4, v_sigma=1e-8, max_norm=1e30)
+    ref, host = _make(w, 0), _make(w, 0)
+    for o in (ref, host):
+        o.init_state(*(synth.make_state(w, k, "cuda") for k in ("master", "m", "v")))
+    fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w.shapes]
+    hfp8 = [torch.zeros(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
+    hsc = torch.zeros(host.nblk, dtype=torch.float32, pin_memory=True)
+    hgs, found = [], []
+    for t in range(1, 5):
+        g = synth.make_grads(w, t, "cuda")
+        if t == 3:
+            g[2][1, 7, 9] = float("nan")
+        hgs.append([x.cpu().pin_memory() for x in g])
+        found.append(ref.step(g, fp8))
+    for hg in hgs:
+        assert host.step_from_host(hg, hfp8, hsc, target_blocks=3, wait=False) is None
+    assert host.finish_host_step() == 0 and host.finish_host_step() is None
+    assert found == [0, 0, 1, 0]
+    assert (host.scaler.scale, host.scaler.step) == (ref.scaler.scale, ref.scaler.step) and ref.scaler.step == 3
+    for name in ("master", "m", "v", "scales"):
+        assert torch.equal(getattr(ref, name).view(torch.int32), getattr(host, name).view(torch.int32)), name
+    for a, b in zip(fp8, hfp8):
+        assert torch.equal(a.cpu(), b)
+    assert torch.equal(hsc, ref.scales.cpu())
+    with pytest.raises(RuntimeError):  # no device-path step while a host step is in flight
+        host.step_from_host(hgs[0], hfp8, hsc, target_blocks=3, wait=False)
+        host.step(synth.make_grads(w, 5, "cuda"), fp8)
+    host.finish_host_step()
+
+
 def test_stats_report_the_step(lib):
     import oracle
     w = synth.workload("tiny", dp=1, rank=0, max_norm=0.05)
