@@ -30,8 +30,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fp8z1_step elements/s and achieved HBM GB/s (fraction of ~8 TB/s) per shard, 1 GB300"
-# bytes the fused step must move per padded element: read grad, master, m, v
-# (16) + write master, m, v (12) + write the E4M3 code (1); plus 4 per block (scale)
+# bytes the step must move per real element: read grad, master, m, v (16) +
+# write master, m, v (12) + write the E4M3 code (1); plus 4 per block (scale).
+# The padding of grad / master / m / v is zero and stays zero, and is not moved;
+# a folded code shard also gets its padding codes (1 byte per padded element).
 STEP_BYTES_PER_ELEM = 29
 STEP_BYTES_PER_BLOCK = 4
 FALLBACK_HBM_GBS = 6800.0
@@ -141,7 +143,8 @@ def bench_ours(args, rank, world, dist):
     if args.experts:
         w = synth.workload(args.workload, dp=1, rank=0,
                            shapes=[(min(e, args.experts), r, c) for e, r, c in w.shapes])
-    opt = ShardOptimizer(w.shapes, dp_size=1, rank=0, device=dev, loss_scale=w.loss_scale,
+    dp, shard_rank = (int(x) for x in args.shard.split(":")) if args.shard else (1, 0)
+    opt = ShardOptimizer(w.shapes, dp_size=dp, rank=shard_rank, device=dev, loss_scale=w.loss_scale,
                          growth_interval=w.growth_interval,
                          **{k: v for k, v in w.hp().items() if k != "loss_scale"})
     for kind, buf in (("master", None), ("m", None), ("v", None)):
@@ -152,7 +155,12 @@ def bench_ours(args, rank, world, dist):
     fp8 = [torch.zeros(s, dtype=torch.uint8, device=dev) for s in w.shapes]
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    n_pad, n_real, nblk = opt.n_padded, opt.n_real, opt.nblk
+    # the shard's blocks, padded elements and real elements (whole buffer: all)
+    nblk = opt.b1 - opt.b0
+    n_pad = nblk * F.BLOCK_ELEMS
+    lut = F.fp8z1_copy_lut(opt.layout)[opt.b0:opt.b1]
+    n_real = int((lut["rows_real"].astype("int64") * lut["cols_real"].astype("int64")).sum())
+    whole = (opt.b0, opt.b1) == (0, opt.nblk)
 
     def stages(path):
         """The kernels of one step on ``path``, as (label, launch) pairs."""
@@ -244,14 +252,14 @@ def bench_ours(args, rank, world, dist):
         del gbuf
 
     peak, peak_kind = _peak_hbm()
-    # algorithmic bytes of the dominant kernel (the fused step): grads read on
-    # the real elements (row-major) or the padded ones (folded), master/m/v read
-    # and written (24 B), one code byte per real (row-major) or padded element
+    # algorithmic bytes of the dominant kernel (the step): grads read and
+    # master/m/v read and written on the real elements, one code byte per real
+    # (row-major codes) or padded (folded codes) element
     if args.path == "fused":
-        step_bytes = 4 * n_real + 24 * n_pad + 1 * n_real + STEP_BYTES_PER_BLOCK * nblk
+        step_bytes = STEP_BYTES_PER_ELEM * n_real + STEP_BYTES_PER_BLOCK * nblk
         gbs = {"fold_norm": 4 * n_real / kern["fold_norm"] / 1e6}
     else:
-        step_bytes = STEP_BYTES_PER_ELEM * n_pad + STEP_BYTES_PER_BLOCK * nblk
+        step_bytes = (STEP_BYTES_PER_ELEM - 1) * n_real + 1 * n_pad + STEP_BYTES_PER_BLOCK * nblk
         gbs = {"fold": 4 * (n_real + n_pad) / kern["fold"] / 1e6, "norm": 4 * n_pad / kern["norm"] / 1e6,
                "unfold": 1 * (n_real + n_pad) / kern["unfold"] / 1e6}
     achieved = step_bytes / (kern["step"] / 1e3) / 1e9
@@ -259,13 +267,38 @@ def bench_ours(args, rank, world, dist):
     tr = _ncu_traffic()
     traffic = None
     if tr and tr.get("workload") == args.workload and tr.get("path") == args.path and \
-            tr.get("source_sha") == _step_source_sha() and not args.experts:
+            tr.get("source_sha") == _step_source_sha() and not args.experts and whole:
         traffic = tr.get("bytes_per_launch")
+
+    # bf16 fold / unfold of the weights over the shard (2-byte elements)
+    bf16 = None
+    if args.bf16_fold:
+        wb = [torch.empty(sh, dtype=torch.bfloat16, device=dev).normal_(0, 0.02) for sh in w.shapes]
+        folded = torch.empty(n_pad, dtype=torch.bfloat16, device=dev)
+        bptrs = opt._ptrs(wb)
+        fold_b = lambda: F.fp8z1_fold(opt.layout, bptrs, folded, 2, opt.b0, opt.b1)  # noqa: E731
+        unfold_b = lambda: F.fp8z1_unfold(opt.layout, folded, bptrs, 2, opt.b0, opt.b1)  # noqa: E731
+        bf16 = {}
+        for name, fn in (("fold", fold_b), ("unfold", unfold_b)):
+            for _ in range(3):
+                fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.bf16_fold)]
+            for a, b in evs:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+            bf16[name + "_ms"] = ms
+            bf16[name + "_gbs"] = 2 * (n_real + n_pad) / ms / 1e6
+        bf16["bytes_per_launch"] = 2 * (n_real + n_pad)
+        del wb, folded
 
     # e2e: the same step through the public API, grads from pinned host memory
     # and the FP8 weights + scales + found flag read back every step
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and whole:
         hgrads = [torch.empty(s, dtype=torch.float32, pin_memory=True) for s in w.shapes]
         for h, d in zip(hgrads, grads):
             h.copy_(d)
@@ -314,7 +347,8 @@ def bench_ours(args, rank, world, dist):
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
         "config": {
             "workload": f"{args.workload}{'' if not args.experts else f'[{args.experts} experts]'}: " + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
-            "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "dp": "whole buffer (1 rank)",
+            "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "dp": "whole buffer (1 rank)" if whole else
+                  f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1}) (this rank's norm partial; no all-reduce on one GPU)",
             "parallelism": f"replicas{world}" if world > 1 else "single",
             "l2": "inputs larger than L2 (~31 GB resident per step), no flush",
             "value_counts": "padded elements per second through the whole step",
@@ -333,6 +367,7 @@ def bench_ours(args, rank, world, dist):
         "clocks": clk,
         "skipped_steps": skipped,
         "e2e": e2e,
+        "bf16_fold": bf16,
     }
     if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)
@@ -424,7 +459,8 @@ def bench_mx(args, rank, world, dist):
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
         "config": {"workload": f"{args.workload} in the MXFP8 layout (E8M0 scale per 32 elements): "
                                + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
-                   "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)",
+                   "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)" if whole else
+                  f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1}) (this rank's norm partial; no all-reduce on one GPU)",
                    "l2": "inputs larger than L2, no flush"},
         "scheme": "mx", "gpu_launches": 2 * args.steps, "kernels_ms": kern,
         "kernels_gbs": {"norm": 4 * n / kern["norm"] / 1e6, "step": achieved},
@@ -537,6 +573,10 @@ def main():
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--bf16-fold", type=int, default=0,
+                    help="also time N launches each of the bf16 fold and unfold of the weights")
+    ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "
+                    "instead of the whole buffer (block scheme)")
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=1)
     args = ap.parse_args()

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfp8z1.so")
-SOURCES = ["layout.cpp", "fold.cu", "norm.cu", "step.cu", "mx.cu"]
+SOURCES = ["layout.cpp", "fold.cu", "norm.cu", "step.cu", "step_full.cu", "step_pad.cu", "mx.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -41,9 +41,9 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, "internal.h"),
-                                                      os.path.join(CSRC, "update.cuh"),
-                                                      os.path.join(INCLUDE, "fp8z1.h")]
+    deps = [os.path.join(CSRC, s) for s in SOURCES] + \
+        [os.path.join(CSRC, h) for h in ("internal.h", "update.cuh", "step_args.h", "step_kernel.cuh")] + \
+        [os.path.join(INCLUDE, "fp8z1.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

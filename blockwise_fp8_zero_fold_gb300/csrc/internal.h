@@ -28,6 +28,10 @@ struct fp8z1_layout {
     unsigned* d_counter = nullptr;     // grad-norm workspace: CTAs finished
     unsigned* d_status = nullptr;      // FP8Z1_DEV_* bits
     int max_partials = 0;
+    // [first, last) block pairs, ascending: runs of at least kFullRunMin blocks
+    // whose params have R and C multiples of 128 (every block a full tile)
+    std::vector<int64_t> full_runs;
+    static constexpr int64_t kFullRunMin = 512;
 };
 
 // MXFP8 layout: the params' row-major elements back to back, cut into groups

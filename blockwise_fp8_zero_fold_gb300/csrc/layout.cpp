@@ -111,6 +111,25 @@ extern "C" int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, i
                     b.cols_real = (int16_t)(cr < kTile ? cr : kTile);
                 }
     }
+    // runs of params made of full tiles only (the step skips no padding there)
+    try {
+        int64_t first = 0, run0 = -1;
+        for (int32_t i = 0; i <= n_params; ++i) {
+            const bool full = i < n_params && shapes[i].R % kTile == 0 && shapes[i].C % kTile == 0;
+            if (full && run0 < 0) run0 = first;
+            if (!full && run0 >= 0) {
+                if (first - run0 >= fp8z1_layout::kFullRunMin) {
+                    L->full_runs.push_back(run0);
+                    L->full_runs.push_back(first);
+                }
+                run0 = -1;
+            }
+            if (i < n_params) first += shapes[i].E * tiles(shapes[i].R) * tiles(shapes[i].C);
+        }
+    } catch (...) {
+        delete L;
+        return FP8Z1_ENOMEM;
+    }
     if (!(flags & FP8Z1_LAYOUT_HOST_ONLY)) {
         const int st = upload(L);
         if (st != FP8Z1_OK) {

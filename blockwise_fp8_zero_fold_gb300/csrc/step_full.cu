@@ -1,0 +1,4 @@
+// The step kernels for blocks that are full 128x128 tiles (no padding test).
+#include "step_kernel.cuh"
+
+template void fp8z1::stepk::launch<false>(const fp8z1::stepk::StepArgs&, int64_t, cudaStream_t, unsigned);

@@ -1,0 +1,300 @@
+// The fused optimizer step over a block range of the shard: unscale + clip +
+// AdamW on the FP32 master/m/v, then the block's scale and E4M3 codes, in one
+// HBM pass.
+//
+// "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结: the optimizer update is
+// elementwise on the rank's slice, and each rank then quantises new FP8 params
+// and their scales from its FP32 master; §Blockwise 量化: one scale per
+// 128x128 block; §参数布局变换: grads are folded to the optimizer's layout and
+// the FP8 params unfolded back.  "DeepSpeed ZeRO 优化" §三: unscale and clip,
+// then the update, then the low-precision copy; §七: clip_coef = max_norm /
+// (||g_s|| / S + 1e-6), applied when < 1; §六: a found inf skips the step.
+//
+// One CTA of 512 threads per block of 16384 elements; thread t owns the
+// float4 chunks t, t+512, ..., t+3584 of the block (chunk i is row i/32,
+// columns 4*(i%32) .. +3 of the 128x128 block, so a warp covers one block row).
+// It streams grad / master / m / v in, updates them, writes master / m / v back
+// at once and keeps its 32 new master values in registers while the CTA
+// reduces the block amax (warp shuffles, then 16 partials in shared memory).
+// The codes are then produced from the registers: no second pass over HBM.
+//
+// Where the grads come from and where the codes go is chosen at compile time:
+//   GRAD_ROWS    grads are read from the row-major params through the block
+//                lookup table (the fold of the grads, fused), else from the
+//                folded grad shard;
+//   CODES_ROWS   codes are written into the row-major FP8 params through the
+//                lookup table (the unfold of the codes, fused);
+//   CODES_FOLDED codes are written to the folded code shard.
+//
+// The FP32 update is update.cuh's; then scale = amax/448 (1 when amax == 0)
+// and code = cvt.rn.satfinite.e4m3(p / scale).
+//
+// Padding: the elements of a block outside its real rows and columns are zero
+// in grad, master, m and v (fold writes them so), and the update maps them to
+// zero again (g = 0 gives m = v = +0 and p = fma(-a, +0, +0) = +0), so a block
+// that is not a full 128x128 tile skips the float4 chunks that hold padding
+// only: no load, no store, new master 0 (which leaves the amax alone), code
+// 0x00 in the folded code shard.  Full tiles take the loop without the test.
+#pragma once
+
+#include <math.h>
+
+#include "step_args.h"
+
+namespace fp8z1 {
+namespace stepk {
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// the 4 grads of chunk (r, c) of a row-major tile; zeros outside the real extent
+__device__ __forceinline__ float4 load_grad_rows(const float* tile, int64_t ld, int r, int c, int rows,
+                                                 int cols, bool vec)
+{
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < rows) {
+        const float* src = tile + r * ld + c;
+        if (vec) {  // ld % 4 == 0: a 4-column group is all real or all padding
+            if (c < cols) g = __ldcs(reinterpret_cast<const float4*>(src));
+        } else {
+            if (c + 0 < cols) g.x = __ldcs(src + 0);
+            if (c + 1 < cols) g.y = __ldcs(src + 1);
+            if (c + 2 < cols) g.z = __ldcs(src + 2);
+            if (c + 3 < cols) g.w = __ldcs(src + 3);
+        }
+    }
+    return g;
+}
+
+__device__ __forceinline__ void store_codes_rows(uint8_t* tile, int64_t ld, int r, int c, int rows,
+                                                 int cols, bool vec, uint32_t q)
+{
+    if (r >= rows) return;
+    uint8_t* dst = tile + r * ld + c;
+    if (vec) {
+        if (c < cols) __stcs(reinterpret_cast<unsigned int*>(dst), q);
+    } else {
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (c + b < cols) dst[b] = (uint8_t)(q >> (8 * b));
+    }
+}
+
+// Quantisation monitors ("FP8训练技术与万亿参数模型优化实践" §1.2: underflow =
+// zeros / total, distortion = cosine(original, dequantised)), per block: the
+// count of non-zero new masters whose code decodes to 0, and
+// sum(p d) / sqrt(sum(p^2) sum(d^2)) with d = decode(code) * scale (1 when both
+// are all zero, 0 when only one is).  FP32 sums per thread, double across the
+// CTA: a diagnostic, not bit-exact.
+__device__ __forceinline__ void monitor_add(float p, float dec, float scale, float& pd, float& pp,
+                                            float& dd, uint32_t& under)
+{
+    const float d = __fmul_rn(dec, scale);
+    pd = __fmaf_rn(p, d, pd);
+    pp = __fmaf_rn(p, p, pp);
+    dd = __fmaf_rn(d, d, dd);
+    under += (p != 0.0f && dec == 0.0f) ? 1u : 0u;
+}
+
+// The update of this thread's 8 float4 chunks of the block: new masters into
+// pn, their largest magnitude into amax.  PAD: skip the chunks that hold
+// padding only (chunk j of thread t is row t/32 + 16 j, columns 4 (t%32) .. +3).
+template <bool GRAD_ROWS, bool PAD>
+__device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, int64_t base,
+                                              int tid, const float* gtile, int64_t ld, int rows, int cols,
+                                              bool gvec, float (&pn)[4 * kVec], float& amax)
+{
+    const int row0 = tid >> 5, col = (tid & 31) << 2;
+    // chunks j < jn hold real elements (rows grow with j, the column does not)
+    int jn = kVec;
+    if (PAD) jn = col >= cols ? 0 : min(kVec, max(0, (rows - row0 + 15) >> 4));
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        if (PAD && j >= jn) {
+            pn[4 * j + 0] = pn[4 * j + 1] = pn[4 * j + 2] = pn[4 * j + 3] = 0.0f;
+            continue;
+        }
+        const int64_t i = base + j * kThreads;
+        float4 g4;
+        if (GRAD_ROWS)
+            g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec);
+        else
+            g4 = __ldcs(a.grad + i);
+        float4 p4 = a.master[i];
+        float4 m4 = a.mom1[i];
+        float4 v4 = a.mom2[i];
+        adamw(gs, c, g4.x, p4.x, m4.x, v4.x);
+        adamw(gs, c, g4.y, p4.y, m4.y, v4.y);
+        adamw(gs, c, g4.z, p4.z, m4.z, v4.z);
+        adamw(gs, c, g4.w, p4.w, m4.w, v4.w);
+        __stcs(a.mom1 + i, m4);
+        __stcs(a.mom2 + i, v4);
+        __stcs(a.master + i, p4);
+        pn[4 * j + 0] = p4.x;
+        pn[4 * j + 1] = p4.y;
+        pn[4 * j + 2] = p4.z;
+        pn[4 * j + 3] = p4.w;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p4.x), fabsf(p4.y)), fmaxf(fabsf(p4.z), fabsf(p4.w))));
+    }
+}
+
+template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, bool DEVSC, bool PAD>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
+{
+    if (*a.found_inf != 0) return;  // skipped step: write nothing
+    __shared__ float s_gscale;
+    __shared__ float s_amax[kWarps];
+    __shared__ StepScalars s_c;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        if (DEVSC) s_c = *a.dsc;
+        s_gscale = grad_factor(*a.sumsq, DEVSC ? s_c : a.c);
+    }
+
+    // the block's place in its row-major param and its real extent
+    const int64_t kb = a.blk_off + blockIdx.x;  // block index from b0
+    int rows = FP8Z1_TILE, cols = FP8Z1_TILE;
+    int64_t ld = 0, off = 0;
+    int param = 0;
+    if (GRAD_ROWS || CODES_ROWS || PAD) {
+        const fp8z1_block blk = a.lut[a.b0 + kb];
+        rows = blk.rows_real;
+        cols = blk.cols_real;
+        ld = blk.ld;
+        off = blk.src_offset;
+        param = blk.param;
+    }
+    const float* gtile = nullptr;
+    bool gvec = false;
+    if (GRAD_ROWS) {
+        const float* base = a.grad_params[param];
+        if (base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0) {
+            if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
+            return;  // uniform: the block is left untouched
+        }
+        gtile = base + off;
+        gvec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(gtile) & 15) == 0);
+    }
+    uint8_t* ctile = nullptr;
+    bool cvec = false;
+    if (CODES_ROWS) {
+        uint8_t* base = a.code_params[param];
+        if (base == nullptr) {
+            if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
+            return;
+        }
+        ctile = base + off;
+        cvec = ((ld & 3) == 0) && ((reinterpret_cast<uintptr_t>(ctile) & 3) == 0);
+    }
+    __syncthreads();
+    const float gs = s_gscale;
+    const StepScalars& c = DEVSC ? s_c : a.c;
+
+    const int64_t base = kb * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+    float pn[4 * kVec];
+    float amax = 0.0f;
+    update_chunks<GRAD_ROWS, PAD>(a, c, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) s_amax[tid >> 5] = amax;
+    __syncthreads();
+    float bmax = s_amax[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) bmax = fmaxf(bmax, s_amax[w]);
+    const float scale = bmax == 0.0f ? 1.0f : __fdiv_rn(bmax, 448.0f);
+    if (tid == 0) a.scales[kb] = scale;
+
+    float pd = 0.0f, pp = 0.0f, dd = 0.0f;
+    uint32_t under = 0u;
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        const uint32_t lo = e4m3x2(__fdiv_rn(pn[4 * j + 0], scale), __fdiv_rn(pn[4 * j + 1], scale));
+        const uint32_t hi = e4m3x2(__fdiv_rn(pn[4 * j + 2], scale), __fdiv_rn(pn[4 * j + 3], scale));
+        const uint32_t q = lo | (hi << 16);
+        if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
+        if (CODES_ROWS) {
+            const int ci = tid + j * kThreads;
+            store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
+        }
+        if (MON) {
+            const float2 d01 = e4m3x2_decode(lo), d23 = e4m3x2_decode(hi);
+            monitor_add(pn[4 * j + 0], d01.x, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 1], d01.y, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 2], d23.x, scale, pd, pp, dd, under);
+            monitor_add(pn[4 * j + 3], d23.y, scale, pd, pp, dd, under);
+        }
+    }
+    if (MON) {
+        __shared__ float s_mon[3][kWarps];
+        __shared__ uint32_t s_under[kWarps];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            pd += __shfl_xor_sync(0xffffffffu, pd, o);
+            pp += __shfl_xor_sync(0xffffffffu, pp, o);
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+            under += __shfl_xor_sync(0xffffffffu, under, o);
+        }
+        if ((tid & 31) == 0) {
+            s_mon[0][tid >> 5] = pd;
+            s_mon[1][tid >> 5] = pp;
+            s_mon[2][tid >> 5] = dd;
+            s_under[tid >> 5] = under;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            double tpd = 0.0, tpp = 0.0, tdd = 0.0;
+            uint32_t tu = 0u;
+            for (int w = 0; w < kWarps; ++w) {
+                tpd += s_mon[0][w];
+                tpp += s_mon[1][w];
+                tdd += s_mon[2][w];
+                tu += s_under[w];
+            }
+            float cosv;
+            if (tpp == 0.0 && tdd == 0.0)
+                cosv = 1.0f;
+            else if (tpp == 0.0 || tdd == 0.0)
+                cosv = 0.0f;
+            else
+                cosv = (float)(tpd / sqrt(tpp * tdd));
+            a.block_cos[kb] = cosv;
+            a.block_underflow[kb] = tu;
+        }
+    }
+}
+
+// `hp` may be null (scalars in device memory); when given it must be in domain
+
+template <bool PAD>
+void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
+{
+    // the forms the entry points use: grads folded or row-major, codes to
+    // the folded shard and/or row-major, with or without monitors, scalars by
+    // value or in device memory
+#define FP8Z1_STEP_FORM(GR, CR, CF, MON, DEV)                                                        \
+    if (forms == ((GR ? kGradRows : 0u) | (CR ? kCodesRows : 0u) | (CF ? kCodesFolded : 0u) |         \
+                  (MON ? kMonitors : 0u) | (DEV ? kDevScalars : 0u))) {                              \
+        step_kernel<GR, CR, CF, MON, DEV, PAD><<<(unsigned)nb, kThreads, 0, s>>>(a);                 \
+        return;                                                                                      \
+    }
+#define FP8Z1_STEP_FORMS_GC(GR, CR, CF)                                                              \
+    FP8Z1_STEP_FORM(GR, CR, CF, false, false)                                                        \
+    FP8Z1_STEP_FORM(GR, CR, CF, false, true)                                                         \
+    FP8Z1_STEP_FORM(GR, CR, CF, true, false)                                                         \
+    FP8Z1_STEP_FORM(GR, CR, CF, true, true)
+    FP8Z1_STEP_FORMS_GC(true, true, true)
+    FP8Z1_STEP_FORMS_GC(true, true, false)
+    FP8Z1_STEP_FORMS_GC(true, false, true)
+    FP8Z1_STEP_FORMS_GC(false, true, true)
+    FP8Z1_STEP_FORMS_GC(false, true, false)
+    FP8Z1_STEP_FORMS_GC(false, false, true)
+#undef FP8Z1_STEP_FORMS_GC
+#undef FP8Z1_STEP_FORM
+}
+
+}  // namespace stepk
+}  // namespace fp8z1

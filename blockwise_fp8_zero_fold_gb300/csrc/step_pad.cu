@@ -1,0 +1,4 @@
+// The step kernels for any block, skipping the float4 chunks that hold padding only.
+#include "step_kernel.cuh"
+
+template void fp8z1::stepk::launch<true>(const fp8z1::stepk::StepArgs&, int64_t, cudaStream_t, unsigned);

@@ -216,6 +216,11 @@ int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks, double* d
  * saturates to +-448, sign kept) to fp8_shard.  When *d_found_inf != 0 the
  * kernel writes nothing (the skipped step of §六): every buffer stays
  * bit-identical.  `grad_shard` is not modified.
+ * Padding: the elements of a block outside its real rows and columns must be
+ * zero in grad_shard, master, m and v, as fp8z1_fold writes them.  The update
+ * maps zero to zero there (g = 0 gives m = v = +0 and p = +0), so the step
+ * neither reads nor writes the padding of those four buffers; fp8_shard gets
+ * code 0x00 in its padding.
  * Pointers: device; grad/master/m/v/fp8 16-byte aligned, scale 4-byte aligned.
  * Errors: EINVAL (null, range, hp out of domain), EALIGN, ENODEV, ECUDA. */
 int fp8z1_step(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float* grad_shard,
@@ -250,7 +255,9 @@ int fp8z1_fold_norm(const fp8z1_layout* layout, const float* const* d_grad_param
  * and/or `d_fp8_params` (DEVICE array of DEVICE pointers to the row-major
  * uint8 FP8 params, written on their real elements only: the fused unfold).
  * Master / m / v / scales and every numerical result are those of
- * fp8z1_step.  A null grad or FP8 param pointer (or a grad pointer that is not
+ * fp8z1_step, and so is the padding contract (padding of master / m / v,
+ * and of grad_shard when given, zero and neither read nor written).  A null
+ * grad or FP8 param pointer (or a grad pointer that is not
  * 4-byte aligned) leaves that block untouched and sets
  * FP8Z1_DEVSTATUS_BADPTR.
  * Quantisation monitors ("FP8训练技术与万亿参数模型优化实践" §1.2: underflow =

@@ -256,3 +256,51 @@ def test_fused_path_with_unaligned_param_views(lib, offset):
         n = int(np.prod(s))
         assert (st[:offset] == 0xEE).all() and (st[offset + n:] == 0xEE).all()  # nothing outside the view
     assert F.fp8z1_device_status(L) == 0
+
+
+@pytest.mark.parametrize("cut", ["whole", "inside_full_run", "across_runs"])
+def test_step_mixes_full_and_padded_runs(lib, cut):
+    """A layout whose 600-block param of full tiles sits between params with
+    padding: the full run goes to the kernel without the padding test, the
+    rest to the one that skips the padding-only chunks.  Every form (folded
+    and row-major) over whole and cut ranges equals the oracle bit for bit,
+    and the padding of master / m / v stays zero."""
+    shapes = [(1, 300, 200), (1, 2560, 3840), (2, 129, 257), (1, 256, 256)]
+    rng = np.random.default_rng(61)
+    L = F.fp8z1_build_layout(shapes)
+    nblk = F.fp8z1_layout_info(L)[0]
+    b0, b1 = {"whole": (0, nblk), "inside_full_run": (50, 400), "across_runs": (3, nblk - 2)}[cut]
+    n = (b1 - b0) * B
+    gh = _rows(shapes, rng, 1024e-3)
+    ph = _rows(shapes, rng, 0.02)
+    mh = _rows(shapes, rng, 1e-4)
+    vh = [np.abs(x) for x in _rows(shapes, rng, 1e-8)]
+    og, op, om, ov = (oracle.fold(shapes, x, b0, b1) for x in (gh, ph, mh, vh))
+    s_exact, fe = oracle.sumsq(og)
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.5,
+              loss_scale=1024.0, step=3)
+    q, oscale, _ = oracle.step(oracle.make_hp(**hp), s_exact, fe, og, op, om, ov)
+    want8 = [np.full(x.shape, 0xEE, np.uint8) for x in gh]
+    oracle.unfold(shapes, q, want8, b0, b1)
+    s = torch.tensor([s_exact], dtype=torch.float64, device="cuda")
+    f = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g = _dev(gh)
+    gf = torch.from_numpy(og).cuda()
+    for grad_rows in (False, True):
+        p_, m_, v_ = (torch.from_numpy(x).cuda() for x in (oracle.fold(shapes, ph, b0, b1),
+                                                            oracle.fold(shapes, mh, b0, b1),
+                                                            oracle.fold(shapes, vh, b0, b1)))
+        sc = torch.empty(b1 - b0, device="cuda")
+        fq = torch.full((n,), 0xEE, dtype=torch.uint8, device="cuda")
+        f8 = [torch.full(x.shape, 0xEE, dtype=torch.uint8, device="cuda") for x in gh]
+        F.fp8z1_step_fused(L, F.make_hp(**hp), grad_shard=None if grad_rows else gf,
+                           d_grad_params=F.param_pointers(g) if grad_rows else None, master_shard=p_,
+                           m_shard=m_, v_shard=v_, fp8_shard=fq, d_fp8_params=F.param_pointers(f8),
+                           scale_shard=sc, b0=b0, b1=b1, d_sumsq=s, d_found_inf=f)
+        torch.cuda.synchronize()
+        for got, want in ((p_, op), (m_, om), (v_, ov), (sc, oscale)):
+            assert np.array_equal(to_host(got).view(np.uint32), want.view(np.uint32))
+        assert np.array_equal(to_host(fq), q)
+        for a, b in zip(f8, want8):
+            assert np.array_equal(to_host(a), b)
+    assert F.fp8z1_device_status(L) == 0
