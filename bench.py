@@ -475,7 +475,7 @@ def _step_source_sha():
     """Hash of the step kernel's sources: its traffic is stale once they change."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("step.cu", "update.cuh"):
+    for name in ("step.cu", "step_args.h", "step_kernel.cuh", "step_full.cu", "step_pad.cu", "update.cuh"):
         with open(os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -13,6 +13,14 @@
 // that meets device data it cannot use (it then skips that work).
 #define FP8Z1_DEV_BADPTR 1u  // a param pointer was null or not elem_size aligned
 
+// A run of at most FP8Z1_BLOCK_ELEMS consecutive row-major elements of one
+// param: what the norm reads for a param that a block range holds whole.
+struct fp8z1_unit {
+    int64_t offset;  // first element, from the param's start
+    int32_t param;
+    int32_t count;   // elements, 1 .. FP8Z1_BLOCK_ELEMS
+};
+
 struct fp8z1_layout {
     std::vector<fp8z1_shape> shapes;
     std::vector<fp8z1_block> lut;  // host copy of the block lookup table
@@ -28,6 +36,10 @@ struct fp8z1_layout {
     unsigned* d_counter = nullptr;     // grad-norm workspace: CTAs finished
     unsigned* d_status = nullptr;      // FP8Z1_DEV_* bits
     int max_partials = 0;
+    std::vector<int64_t> param_block0;  // first block of each param; n_params + 1 entries
+    std::vector<int64_t> param_unit0;   // first unit of each param; n_params + 1 entries
+    std::vector<fp8z1_unit> units;      // every param cut into units, in param order
+    fp8z1_unit* d_units = nullptr;      // device copy of `units`
     // [first, last) block pairs, ascending: runs of at least kFullRunMin blocks
     // whose params have R and C multiples of 128 (every block a full tile)
     std::vector<int64_t> full_runs;

@@ -23,10 +23,12 @@ int64_t tiles(int64_t n) { return (n + kTile - 1) / kTile; }
 void release_device(fp8z1_layout* L)
 {
     cudaFree(L->d_lut);
+    cudaFree(L->d_units);
     cudaFree(L->d_partials);
     cudaFree(L->d_counter);
     cudaFree(L->d_status);
     L->d_lut = nullptr;
+    L->d_units = nullptr;
     L->d_partials = nullptr;
     L->d_counter = nullptr;
     L->d_status = nullptr;
@@ -40,7 +42,9 @@ int upload(fp8z1_layout* L)
     // grad-norm workspace: up to 4 CTAs per SM, capped at 4096 partial sums
     L->max_partials = L->sm_count * 4 < 4096 ? L->sm_count * 4 : 4096;
     const size_t lut_bytes = sizeof(fp8z1_block) * (size_t)L->n_blocks;
+    const size_t unit_bytes = sizeof(fp8z1_unit) * L->units.size();
     if (cudaMalloc(&L->d_lut, lut_bytes ? lut_bytes : sizeof(fp8z1_block)) != cudaSuccess ||
+        cudaMalloc(&L->d_units, unit_bytes ? unit_bytes : sizeof(fp8z1_unit)) != cudaSuccess ||
         cudaMalloc(&L->d_partials, sizeof(double) * (size_t)L->max_partials) != cudaSuccess ||
         cudaMalloc(&L->d_counter, sizeof(unsigned)) != cudaSuccess ||
         cudaMalloc(&L->d_status, sizeof(unsigned)) != cudaSuccess) {
@@ -48,6 +52,8 @@ int upload(fp8z1_layout* L)
         return FP8Z1_ENOMEM;
     }
     if (lut_bytes && cudaMemcpy(L->d_lut, L->lut.data(), lut_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
+        return FP8Z1_ECUDA;
+    if (unit_bytes && cudaMemcpy(L->d_units, L->units.data(), unit_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
         return FP8Z1_ECUDA;
     if (cudaMemset(L->d_counter, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(L->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
@@ -113,6 +119,24 @@ extern "C" int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, i
     }
     // runs of params made of full tiles only (the step skips no padding there)
     try {
+        // each param's first block, and its row-major elements cut into units
+        L->param_block0.resize((size_t)n_params + 1);
+        L->param_unit0.resize((size_t)n_params + 1);
+        int64_t nunits = 0;
+        for (int32_t i = 0; i < n_params; ++i)
+            nunits += (shapes[i].E * shapes[i].R * shapes[i].C + FP8Z1_BLOCK_ELEMS - 1) / FP8Z1_BLOCK_ELEMS;
+        L->units.reserve((size_t)nunits);
+        int64_t b = 0;
+        for (int32_t i = 0; i < n_params; ++i) {
+            L->param_block0[(size_t)i] = b;
+            L->param_unit0[(size_t)i] = (int64_t)L->units.size();
+            b += shapes[i].E * tiles(shapes[i].R) * tiles(shapes[i].C);
+            const int64_t n = shapes[i].E * shapes[i].R * shapes[i].C;
+            for (int64_t o = 0; o < n; o += FP8Z1_BLOCK_ELEMS)
+                L->units.push_back({o, i, (int32_t)(n - o < FP8Z1_BLOCK_ELEMS ? n - o : FP8Z1_BLOCK_ELEMS)});
+        }
+        L->param_block0[(size_t)n_params] = b;
+        L->param_unit0[(size_t)n_params] = (int64_t)L->units.size();
         int64_t first = 0, run0 = -1;
         for (int32_t i = 0; i <= n_params; ++i) {
             const bool full = i < n_params && shapes[i].R % kTile == 0 && shapes[i].C % kTile == 0;

@@ -32,6 +32,7 @@
 // The result is deterministic for a given device and range.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -107,13 +108,20 @@ __device__ __forceinline__ void sum_block(const float4 (&x)[kVec], double& acc, 
     }
 }
 
-// Where block k's grads live in the row-major params.
+// Where the grads of one unit of work come from: the folded shard, a block of
+// the row-major params (through the block table), or a run of at most 16384
+// consecutive elements of one row-major param (a param the range holds whole:
+// its sum of squares needs no block structure).
+enum Src { kFolded, kRows, kParams };
+
+// Where unit k's grads live in the row-major params.
 struct RowSrc {
     const float* tile;
     int64_t ld;
     int rows, cols;
-    bool vec;  // 16-byte loads (ld % 4 == 0 and an aligned tile)
-    bool bad;  // null or misaligned param pointer
+    int count;  // kParams: elements in the run
+    bool vec;   // 16-byte loads (kRows: ld % 4 == 0 and an aligned tile; kParams: an aligned run)
+    bool bad;   // null or misaligned param pointer
 };
 
 __device__ __forceinline__ RowSrc row_src(const fp8z1_block* __restrict__ lut,
@@ -131,14 +139,28 @@ __device__ __forceinline__ RowSrc row_src(const fp8z1_block* __restrict__ lut,
     return s;
 }
 
+__device__ __forceinline__ RowSrc param_src(const fp8z1_unit* __restrict__ units,
+                                            const float* const* __restrict__ params, int64_t u)
+{
+    const fp8z1_unit un = units[u];
+    const float* base = params[un.param];
+    RowSrc s = {};
+    s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
+    s.tile = s.bad ? nullptr : base + un.offset;
+    s.count = un.count;
+    s.vec = !s.bad && (reinterpret_cast<uintptr_t>(s.tile) & 15) == 0;
+    return s;
+}
+
 struct NormArgs {
-    const float4* g;              // folded grads at block b0 (!ROWS)
-    const fp8z1_block* lut;       // ROWS
-    const float* const* params;   // ROWS: row-major FP32 grads
+    const float4* g;              // folded grads at block b0 (kFolded)
+    const fp8z1_block* lut;       // kRows
+    const fp8z1_unit* units;      // kParams
+    const float* const* params;   // kRows, kParams: row-major FP32 grads
     float4* store;                // STORE: folded grads at block b0
-    int64_t b0;                   // first block (ROWS: LUT index)
+    int64_t b0;                   // first block (kRows: LUT index) or unit (kParams)
     int64_t nblocks;              // blocks of 16384, the last one possibly partial
-    int64_t tail_k;               // !ROWS: index of a partial last block ...
+    int64_t tail_k;               // kFolded: index of a partial last block ...
     int tail_vec4;                // ... and its float4 count (0: no partial block)
     double* partials;             // one per CTA
     unsigned* counter;
@@ -147,14 +169,15 @@ struct NormArgs {
     int32_t* found_inf;
 };
 
-// Issue the loads of block k (index from b0): this thread's 32 values.  Chunk
-// j is tid + 512 j: block row (tid + 512 j) / 32, columns 4 * ((tid + 512 j)
-// % 32) .. + 3.  Zeros outside the real extent.
-template <bool ROWS>
+// Issue the loads of unit k (index from b0): this thread's 32 values.  For a
+// block, chunk j is tid + 512 j: block row (tid + 512 j) / 32, columns
+// 4 * ((tid + 512 j) % 32) .. + 3; for a run of a param, elements
+// 4 (tid + 512 j) .. + 3.  Zeros outside the real extent.
+template <Src SRC>
 __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
                                            float4 (&x)[kVec])
 {
-    if constexpr (!ROWS) {
+    if constexpr (SRC == kFolded) {
         const float4* p = a.g + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
         if (a.tail_vec4 != 0 && k == a.tail_k) {  // a flat range's partial last block
 #pragma unroll
@@ -165,6 +188,30 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
         }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+    } else if constexpr (SRC == kParams) {
+        if (s.vec && s.count == FP8Z1_BLOCK_ELEMS) {  // a whole, aligned run
+            const float4* p = reinterpret_cast<const float4*>(s.tile) + tid;
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const int e = 4 * (tid + j * kThreads);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!s.bad && e < s.count) {
+                const float* src = s.tile + e;
+                if (s.vec && e + 4 <= s.count) {
+                    v = __ldcs(reinterpret_cast<const float4*>(src));
+                } else {
+                    v.x = __ldcs(src + 0);
+                    if (e + 1 < s.count) v.y = __ldcs(src + 1);
+                    if (e + 2 < s.count) v.z = __ldcs(src + 2);
+                    if (e + 3 < s.count) v.w = __ldcs(src + 3);
+                }
+            }
+            x[j] = v;
+        }
     } else {
         if (s.vec && s.rows == FP8Z1_TILE && s.cols == FP8Z1_TILE) {
             // a full, aligned block: chunk j sits 16 rows below chunk j-1
@@ -195,19 +242,20 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
     }
 }
 
-template <bool ROWS>
+template <Src SRC>
 __device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t k)
 {
-    if (ROWS) return row_src(a.lut, a.params, a.b0 + k);
+    if (SRC == kRows) return row_src(a.lut, a.params, a.b0 + k);
+    if (SRC == kParams) return param_src(a.units, a.params, a.b0 + k);
     return RowSrc{};
 }
 
-// Sum (and store) block k, whose values are in x.
-template <bool ROWS, bool STORE>
+// Sum (and store) unit k, whose values are in x.
+template <Src SRC, bool STORE>
 __device__ __forceinline__ void finish_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
                                              const float4 (&x)[kVec], double& acc, int& bad)
 {
-    if (ROWS && s.bad) {  // unreadable grads: nothing is summed or stored
+    if (SRC != kFolded && s.bad) {  // unreadable grads: nothing is summed or stored
         if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
         bad = 1;          // raise found_inf so the step is skipped
         return;
@@ -220,7 +268,7 @@ __device__ __forceinline__ void finish_block(const NormArgs& a, const RowSrc& s,
     sum_block(x, acc, bad);
 }
 
-template <bool ROWS, bool STORE>
+template <Src SRC, bool STORE>
 __global__ void __launch_bounds__(kThreads, 1) norm_kernel(const NormArgs a)
 {
     __shared__ double s_part[kWarps];
@@ -237,21 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1) norm_kernel(const NormArgs a)
     RowSrc sa = {}, sb = {};
     int64_t k = k0;
     if (k < k1) {
-        sa = src_of<ROWS>(a, k);
-        load_block<ROWS>(a, sa, k, tid, xa);
-        if (k + 1 < k1) sb = src_of<ROWS>(a, k + 1);
+        sa = src_of<SRC>(a, k);
+        load_block<SRC>(a, sa, k, tid, xa);
+        if (k + 1 < k1) sb = src_of<SRC>(a, k + 1);
     }
     while (k < k1) {
-        if (k + 1 < k1) load_block<ROWS>(a, sb, k + 1, tid, xb);
+        if (k + 1 < k1) load_block<SRC>(a, sb, k + 1, tid, xb);
         RowSrc sc = {};
-        if (k + 2 < k1) sc = src_of<ROWS>(a, k + 2);
-        finish_block<ROWS, STORE>(a, sa, k, tid, xa, acc, bad);
+        if (k + 2 < k1) sc = src_of<SRC>(a, k + 2);
+        finish_block<SRC, STORE>(a, sa, k, tid, xa, acc, bad);
         if (++k >= k1) break;
         // xb holds block k, sb = where it lives, sc = where block k+1 lives
-        if (k + 1 < k1) load_block<ROWS>(a, sc, k + 1, tid, xa);
+        if (k + 1 < k1) load_block<SRC>(a, sc, k + 1, tid, xa);
         RowSrc sd = {};
-        if (k + 2 < k1) sd = src_of<ROWS>(a, k + 2);
-        finish_block<ROWS, STORE>(a, sb, k, tid, xb, acc, bad);
+        if (k + 2 < k1) sd = src_of<SRC>(a, k + 2);
+        finish_block<SRC, STORE>(a, sb, k, tid, xb, acc, bad);
         ++k;
         sa = sc;
         sb = sd;
@@ -320,7 +368,7 @@ extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, i
     a.status = L->d_status;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
-    norm_kernel<false, false><<<(unsigned)persistent_grid(L, n), kThreads, 0,
+    norm_kernel<kFolded, false><<<(unsigned)persistent_grid(L, n), kThreads, 0,
                                  static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
@@ -339,21 +387,44 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
     if (n == 0) return FP8Z1_OK;
     NormArgs a = {};
     a.lut = L->d_lut;
+    a.units = L->d_units;
     a.params = d_grad_params;
     a.store = reinterpret_cast<float4*>(grad_shard);
-    a.b0 = b0;
-    a.nblocks = n;
     a.partials = L->d_partials;
     a.counter = L->d_counter;
     a.status = L->d_status;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
-    const unsigned grid = (unsigned)persistent_grid(L, n);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (grad_shard)
-        norm_kernel<true, true><<<grid, kThreads, 0, s>>>(a);
-    else
-        norm_kernel<true, false><<<grid, kThreads, 0, s>>>(a);
+    auto blocks = [&](int64_t k0, int64_t k1) {  // through the block table
+        if (k0 == k1) return;
+        a.b0 = k0;
+        a.nblocks = k1 - k0;
+        const unsigned grid = (unsigned)persistent_grid(L, k1 - k0);
+        if (grad_shard) {
+            a.store = reinterpret_cast<float4*>(grad_shard) + (k0 - b0) * (FP8Z1_BLOCK_ELEMS / 4);
+            norm_kernel<kRows, true><<<grid, kThreads, 0, s>>>(a);
+        } else {
+            norm_kernel<kRows, false><<<grid, kThreads, 0, s>>>(a);
+        }
+    };
+    // Without the store, the params the range holds whole are read as flat
+    // runs of their row-major elements (a sum of squares needs no blocks);
+    // the cut params at either end go through the block table.  The pieces
+    // are separate launches on one stream, each adding its total to *d_sumsq.
+    const std::vector<int64_t>& pb = L->param_block0;
+    const int64_t pa = std::lower_bound(pb.begin(), pb.end(), b0) - pb.begin();        // first whole param
+    const int64_t pz = std::upper_bound(pb.begin(), pb.end(), b1) - pb.begin() - 1;    // one past the last
+    if (grad_shard || pa >= pz) {
+        blocks(b0, b1);
+    } else {
+        blocks(b0, pb[(size_t)pa]);
+        const int64_t u0 = L->param_unit0[(size_t)pa], u1 = L->param_unit0[(size_t)pz];
+        a.b0 = u0;
+        a.nblocks = u1 - u0;
+        norm_kernel<kParams, false><<<(unsigned)persistent_grid(L, u1 - u0), kThreads, 0, s>>>(a);
+        blocks(pb[(size_t)pz], b1);
+    }
     return fp8z1::launch_status();
 }
 
@@ -384,7 +455,7 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
     int64_t grid = L->sm_count;
     if (grid > a.nblocks) grid = a.nblocks;
     if (grid > L->max_partials) grid = L->max_partials;
-    norm_kernel<false, false><<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
 
@@ -466,6 +537,6 @@ extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
     const int64_t grid = (n_blocks + kNoAllocBlocksPerCta - 1) / kNoAllocBlocksPerCta;
-    norm_kernel<false, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
+    norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();
 }
