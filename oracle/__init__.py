@@ -69,45 +69,43 @@ class ScalerState(C.Structure):
 
 def _bind(L):
     """Declare the C signatures on a loaded oracle library."""
-    if True:
-        if True:
-            P = C.c_void_p
-            i64, i32 = C.c_int64, C.c_int32
-            L.oracle_count_blocks.argtypes = [C.POINTER(Shape), i32]
-            L.oracle_count_blocks.restype = i64
-            L.oracle_build_lut.argtypes = [C.POINTER(Shape), i32, C.POINTER(Block)]
-            L.oracle_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
-            L.oracle_fold.argtypes = [C.POINTER(Shape), i32, C.POINTER(P), P, i32, i64, i64]
-            L.oracle_fold.restype = C.c_int
-            L.oracle_unfold.argtypes = [C.POINTER(Shape), i32, P, C.POINTER(P), i32, i64, i64]
-            L.oracle_unfold.restype = C.c_int
-            L.oracle_acc_init.argtypes = [C.POINTER(Acc)]
-            L.oracle_acc_add.argtypes = [C.POINTER(Acc), P, i64]
-            L.oracle_acc_merge.argtypes = [C.POINTER(Acc), C.POINTER(Acc)]
-            L.oracle_acc_result.argtypes = [C.POINTER(Acc)]
-            L.oracle_acc_result.restype = C.c_double
-            L.oracle_sumsq.argtypes = [P, i64, C.POINTER(C.c_double), C.POINTER(i32)]
-            L.oracle_clip_coef.argtypes = [C.c_double, C.c_float, C.c_float,
-                                           C.POINTER(C.c_double), C.POINTER(C.c_double),
-                                           C.POINTER(i32)]
-            L.oracle_e4m3_encode.argtypes = [C.c_float]
-            L.oracle_e4m3_encode.restype = C.c_uint8
-            L.oracle_e4m3_decode.argtypes = [C.c_uint8]
-            L.oracle_e4m3_decode.restype = C.c_float
-            L.oracle_e4m3_encode_n.argtypes = [P, P, i64]
-            L.oracle_e4m3_decode_n.argtypes = [P, P, i64]
-            L.oracle_quantise_block.argtypes = [P, P, C.POINTER(C.c_float)]
-            L.oracle_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
-            L.oracle_step.restype = C.c_int
-            L.oracle_scaler_update.argtypes = [C.POINTER(ScalerState), i32]
-            L.oracle_paramwise_split.argtypes = [C.POINTER(Shape), i32, i32, P, P]
-            L.oracle_quant_monitor.argtypes = [P, P, C.c_float, i64, C.POINTER(C.c_double),
-                                               C.POINTER(i64)]
-            L.oracle_e8m0_decode.argtypes = [C.c_uint8]
-            L.oracle_e8m0_decode.restype = C.c_float
-            L.oracle_mx_quantise_group.argtypes = [P, P, P]
-            L.oracle_mx_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
-            L.oracle_mx_step.restype = C.c_int
+    P = C.c_void_p
+    i64, i32 = C.c_int64, C.c_int32
+    L.oracle_count_blocks.argtypes = [C.POINTER(Shape), i32]
+    L.oracle_count_blocks.restype = i64
+    L.oracle_build_lut.argtypes = [C.POINTER(Shape), i32, C.POINTER(Block)]
+    L.oracle_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
+    L.oracle_fold.argtypes = [C.POINTER(Shape), i32, C.POINTER(P), P, i32, i64, i64]
+    L.oracle_fold.restype = C.c_int
+    L.oracle_unfold.argtypes = [C.POINTER(Shape), i32, P, C.POINTER(P), i32, i64, i64]
+    L.oracle_unfold.restype = C.c_int
+    L.oracle_acc_init.argtypes = [C.POINTER(Acc)]
+    L.oracle_acc_add.argtypes = [C.POINTER(Acc), P, i64]
+    L.oracle_acc_merge.argtypes = [C.POINTER(Acc), C.POINTER(Acc)]
+    L.oracle_acc_result.argtypes = [C.POINTER(Acc)]
+    L.oracle_acc_result.restype = C.c_double
+    L.oracle_sumsq.argtypes = [P, i64, C.POINTER(C.c_double), C.POINTER(i32)]
+    L.oracle_clip_coef.argtypes = [C.c_double, C.c_float, C.c_float,
+                                   C.POINTER(C.c_double), C.POINTER(C.c_double),
+                                   C.POINTER(i32)]
+    L.oracle_e4m3_encode.argtypes = [C.c_float]
+    L.oracle_e4m3_encode.restype = C.c_uint8
+    L.oracle_e4m3_decode.argtypes = [C.c_uint8]
+    L.oracle_e4m3_decode.restype = C.c_float
+    L.oracle_e4m3_encode_n.argtypes = [P, P, i64]
+    L.oracle_e4m3_decode_n.argtypes = [P, P, i64]
+    L.oracle_quantise_block.argtypes = [P, P, C.POINTER(C.c_float)]
+    L.oracle_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
+    L.oracle_step.restype = C.c_int
+    L.oracle_scaler_update.argtypes = [C.POINTER(ScalerState), i32]
+    L.oracle_paramwise_split.argtypes = [C.POINTER(Shape), i32, i32, P, P]
+    L.oracle_quant_monitor.argtypes = [P, P, C.c_float, i64, C.POINTER(C.c_double),
+                                       C.POINTER(i64)]
+    L.oracle_e8m0_decode.argtypes = [C.c_uint8]
+    L.oracle_e8m0_decode.restype = C.c_float
+    L.oracle_mx_quantise_group.argtypes = [P, P, P]
+    L.oracle_mx_step.argtypes = [C.POINTER(HP), C.c_double, i32, P, P, P, P, P, P, i64]
+    L.oracle_mx_step.restype = C.c_int
     return L
 
 
