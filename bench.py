@@ -218,14 +218,16 @@ def bench_ours(args, rank, world, dist):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         torch.cuda.nvtx.range_push("timed")
+        n0 = F.fp8z1_kernel_launches()
         t0.record(stream)
         sk = run_steps(path, k, ev)
         t1.record(stream)
+        launches = F.fp8z1_kernel_launches() - n0
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
         kern = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
-        return ms, kern, sk
+        return ms, kern, sk, launches
 
     gptrs = opt._ptrs(grads)
     fptrs = opt._ptrs(fp8)
@@ -238,7 +240,7 @@ def bench_ours(args, rank, world, dist):
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    elapsed_ms, kern, skipped = timed(args.path, args.steps)
+    elapsed_ms, kern, skipped, launches = timed(args.path, args.steps)
     clk = clocks.stop()
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(n_pad, world, args.steps, elapsed_ms / 1e3)
@@ -246,7 +248,7 @@ def bench_ours(args, rank, world, dist):
     if args.compare:
         alt = "unfused" if args.path == "fused" else "fused"
         run_steps(alt, 2)
-        a_ms, a_kern, _ = timed(alt, max(3, args.steps // 4))
+        a_ms, a_kern, _, _ = timed(alt, max(3, args.steps // 4))
         other = {"path": alt, "ms_per_step": a_ms / max(3, args.steps // 4), "kernels_ms": a_kern}
     if gbuf is not None:
         del gbuf
@@ -353,7 +355,7 @@ def bench_ours(args, rank, world, dist):
             "l2": "inputs larger than L2 (~31 GB resident per step), no flush",
             "value_counts": "padded elements per second through the whole step",
         },
-        "gpu_launches": (3 if args.path == "fused" else 4) * args.steps,
+        "gpu_launches": launches,
         "path": args.path,
         "kernels_ms": kern,
         "kernels_gbs": gbs,
@@ -427,6 +429,7 @@ def bench_mx(args, rank, world, dist):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("timed")
+    n0 = F.fp8z1_kernel_launches()
     t0.record(stream)
     skipped = 0
     for i in range(args.steps):
@@ -442,6 +445,7 @@ def bench_mx(args, rank, world, dist):
         ev["step"][i][1].record(stream)
         skipped += opt.finish_step()
     t1.record(stream)
+    launches = F.fp8z1_kernel_launches() - n0
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -459,10 +463,9 @@ def bench_mx(args, rank, world, dist):
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
         "config": {"workload": f"{args.workload} in the MXFP8 layout (E8M0 scale per 32 elements): "
                                + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
-                   "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)" if whole else
-                  f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1}) (this rank's norm partial; no all-reduce on one GPU)",
+                   "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)",
                    "l2": "inputs larger than L2, no flush"},
-        "scheme": "mx", "gpu_launches": 2 * args.steps, "kernels_ms": kern,
+        "scheme": "mx", "gpu_launches": launches, "kernels_ms": kern,
         "kernels_gbs": {"norm": 4 * n / kern["norm"] / 1e6, "step": achieved},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "kernel": "fp8z1_mx_step",
@@ -472,10 +475,11 @@ def bench_mx(args, rank, world, dist):
 
 
 def _step_source_sha():
-    """Hash of the step kernel's sources: its traffic is stale once they change."""
+    """Hash of the files holding the step kernel's device code (the entry
+    points in step.cu are host code): its traffic is stale once they change."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("step.cu", "step_args.h", "step_kernel.cuh", "step_full.cu", "step_pad.cu", "update.cuh"):
+    for name in ("step_args.h", "step_kernel.cuh", "step_full.cu", "step_pad.cu", "update.cuh"):
         with open(os.path.join(ROOT, "blockwise_fp8_zero_fold_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -116,6 +116,7 @@ int launch(const fp8z1_layout* L, void* const* params, uint8_t* shard, int32_t e
 {
     const int64_t n = b1 - b0;
     const dim3 grid((unsigned)n), block(kThreads);
+    fp8z1::count_launch();
     switch (esz) {
     case 1: fold_kernel<1, FOLD><<<grid, block, 0, stream>>>(L->d_lut, params, shard, b0, L->d_status); break;
     case 2: fold_kernel<2, FOLD><<<grid, block, 0, stream>>>(L->d_lut, params, shard, b0, L->d_status); break;

@@ -5,6 +5,7 @@
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <vector>
 
 #include "fp8z1.h"
@@ -84,6 +85,11 @@ struct NvtxRange {
     NvtxRange(const NvtxRange&) = delete;
     NvtxRange& operator=(const NvtxRange&) = delete;
 };
+
+// Kernels this library has enqueued in this process (every device and stream),
+// read through fp8z1_kernel_launches.
+std::atomic<uint64_t>& launch_counter();
+inline void count_launch() { launch_counter().fetch_add(1, std::memory_order_relaxed); }
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

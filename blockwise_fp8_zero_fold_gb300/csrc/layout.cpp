@@ -166,6 +166,19 @@ extern "C" int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, i
     return FP8Z1_OK;
 }
 
+std::atomic<uint64_t>& fp8z1::launch_counter()
+{
+    static std::atomic<uint64_t> n{0};
+    return n;
+}
+
+extern "C" int fp8z1_kernel_launches(uint64_t* out)
+{
+    if (!out) return FP8Z1_EINVAL;
+    *out = fp8z1::launch_counter().load(std::memory_order_relaxed);
+    return FP8Z1_OK;
+}
+
 extern "C" int fp8z1_destroy_layout(fp8z1_layout* L)
 {
     if (!L) return FP8Z1_OK;

@@ -133,6 +133,7 @@ extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp,
     int64_t grid = (int64_t)L->sm_count * 8;
     const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
     if (grid > need) grid = need;
+    fp8z1::count_launch();
     mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }

@@ -368,6 +368,7 @@ extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, i
     a.status = L->d_status;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
+    fp8z1::count_launch();
     norm_kernel<kFolded, false><<<(unsigned)persistent_grid(L, n), kThreads, 0,
                                  static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
@@ -401,6 +402,7 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
         a.b0 = k0;
         a.nblocks = k1 - k0;
         const unsigned grid = (unsigned)persistent_grid(L, k1 - k0);
+        fp8z1::count_launch();
         if (grad_shard) {
             a.store = reinterpret_cast<float4*>(grad_shard) + (k0 - b0) * (FP8Z1_BLOCK_ELEMS / 4);
             norm_kernel<kRows, true><<<grid, kThreads, 0, s>>>(a);
@@ -422,6 +424,7 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
         const int64_t u0 = L->param_unit0[(size_t)pa], u1 = L->param_unit0[(size_t)pz];
         a.b0 = u0;
         a.nblocks = u1 - u0;
+        fp8z1::count_launch();
         norm_kernel<kParams, false><<<(unsigned)persistent_grid(L, u1 - u0), kThreads, 0, s>>>(a);
         blocks(pb[(size_t)pz], b1);
     }
@@ -455,6 +458,7 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
     int64_t grid = L->sm_count;
     if (grid > a.nblocks) grid = a.nblocks;
     if (grid > L->max_partials) grid = L->max_partials;
+    fp8z1::count_launch();
     norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
@@ -537,6 +541,7 @@ extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
     const int64_t grid = (n_blocks + kNoAllocBlocksPerCta - 1) / kNoAllocBlocksPerCta;
+    fp8z1::count_launch();
     norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();
 }

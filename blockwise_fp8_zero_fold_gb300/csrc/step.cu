@@ -37,6 +37,7 @@ void launch_segments(const fp8z1_layout* L, StepArgs a, int64_t b0, int64_t b1, 
                      unsigned forms)
 {
     auto one = [&](int64_t k0, int64_t k1, bool pad) {
+        fp8z1::count_launch();
         a.blk_off = k0 - b0;
         if (pad)
             launch<true>(a, k1 - k0, s, forms);

@@ -102,6 +102,7 @@ _SIGS = {
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
     "fp8z1_clip_coef": (C.c_int, [C.c_double, C.c_float, C.c_float, C.POINTER(C.c_double),
                                   C.POINTER(C.c_double)]),
+    "fp8z1_kernel_launches": (C.c_int, [C.POINTER(C.c_uint64)]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
 
@@ -315,6 +316,13 @@ def fp8z1_step_scalars_from_hp(hp: fp8z1_adamw_hp, out=None) -> fp8z1_step_scala
     if out is not None:
         C.memmove(_ptr(out), C.addressof(sc), C.sizeof(sc))
     return sc
+
+
+def fp8z1_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    n = C.c_uint64()
+    _check(lib().fp8z1_kernel_launches(C.byref(n)), "fp8z1_kernel_launches")
+    return n.value
 
 
 def fp8z1_paramwise_split(shapes, dp_size: int):

@@ -308,6 +308,15 @@ int fp8z1_step_fused_dev(const fp8z1_layout* layout, const fp8z1_step_scalars* h
                          uint32_t* block_underflow, int64_t b0, int64_t b1, const double* d_sumsq,
                          const int32_t* d_found_inf, void* stream);
 
+/* ---- tracing (host only) --------------------------------------------------- */
+
+/* The number of kernels this library has enqueued in this process, on every
+ * device and stream, since it was loaded: the difference across a region of
+ * calls is the launch count of that region.  A launch made while a stream is
+ * being captured counts once, at capture; graph replays do not count.
+ * Errors: EINVAL (null). */
+int fp8z1_kernel_launches(uint64_t* out);
+
 /* ---- param-wise split (§参数粒度切分; host only) ---------------------------- */
 
 /* The page's alternative to the block-wise split, for comparing padding

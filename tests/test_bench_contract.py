@@ -1,0 +1,79 @@
+"""bench.py keeps its JSON-line contract: one line with the metric, the
+whole-job value, the roofline of the dominant kernel, the end-to-end number,
+the clocks seen, the launch count and the CPU (oracle) baseline; the
+reference arm (the oracle on the host cores) prints the same metric."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*args, timeout=900):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+             "scaling", "vs_baseline", "dtype", "data", "config", "e2e"}
+
+
+def test_reference_arm_line():
+    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1")
+    assert BASE_KEYS <= set(d) and d["impl"] == "reference"
+    assert d["value"] > 0 and d["unit"] == "elem/s" and d["higher_is_better"] is True
+    assert d["steps"] == 2 and d["n_gpus"] == 1 and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"]
+
+
+def _check_ours(d, steps):
+    assert BASE_KEYS <= set(d) and "impl" not in d
+    assert d["value"] > 0 and d["steps"] == steps and d["warmup"] >= 3
+    assert d["scaling"] == "weak" and d["n_gpus"] == 1
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"])
+    assert "traffic" in rf
+    ck = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(ck)
+    assert d["gpu_launches"] > 0
+    assert "workload" in d["config"]
+
+
+@pytest.mark.gpu
+def test_bench_line_tiny():
+    d = _run("--workload", "tiny", "--steps", "4", "--warmup", "3", "--compare", "1", "--e2e-steps", "2",
+             "--cpu-sample-experts", "1")
+    _check_ours(d, 4)
+    e = d["e2e"]
+    assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
+    assert d["other_path"]["path"] == "unfused"
+    assert d["gpu_launches"] == 2 * 4  # the flat-run norm and one step launch per step
+
+
+@pytest.mark.gpu
+def test_bench_line_shard_and_bf16_fold():
+    d = _run("--workload", "dense", "--shard", "4:1", "--steps", "3", "--warmup", "3", "--compare", "0",
+             "--e2e-steps", "0", "--cpu-sample-experts", "0", "--bf16-fold", "2")
+    _check_ours(d, 3)
+    assert d["config"]["dp"].startswith("rank 1 of 4")
+    assert d["config"]["blocks"] == 3760 and d["e2e"] is None
+    assert d["bf16_fold"]["fold_ms"] > 0 and d["bf16_fold"]["unfold_ms"] > 0
+
+
+@pytest.mark.gpu
+def test_bench_line_mx():
+    d = _run("--scheme", "mx", "--workload", "moe", "--experts", "1", "--steps", "3", "--warmup", "3")
+    _check_ours(d, 3)

@@ -197,6 +197,17 @@ def test_clip_coef_host_matches_oracle_and_golden(row):
         F.fp8z1_clip_coef(-1.0, 1.0, 1.0)
 
 
+def test_kernel_launch_counter_host():
+    """Host-only calls launch nothing; a refused device call launches nothing."""
+    n0 = F.fp8z1_kernel_launches()
+    L = F.fp8z1_build_layout([(1, 300, 200)], host_only=True)
+    F.fp8z1_layout_info(L)
+    buf = np.zeros(64, np.uint8)
+    assert F.lib().fp8z1_fold(L.handle, buf.ctypes.data, buf.ctypes.data, 4, 0, 1, None) == F.ENODEV
+    assert F.fp8z1_kernel_launches() == n0
+    assert F.lib().fp8z1_kernel_launches(None) == F.EINVAL
+
+
 def test_step_scalars_from_hp():
     """The per-step FP32 scalars: each formed in double and rounded once."""
     lr, b1, b2, eps, wd, mx, ls, t = 3e-4, 0.9, 0.95, 1e-8, 0.1, 1.0, 4096.0, 7

@@ -304,10 +304,13 @@ def test_step_mixes_full_and_padded_runs(lib, cut):
         sc = torch.empty(b1 - b0, device="cuda")
         fq = torch.full((n,), 0xEE, dtype=torch.uint8, device="cuda")
         f8 = [torch.full(x.shape, 0xEE, dtype=torch.uint8, device="cuda") for x in gh]
+        n0 = F.fp8z1_kernel_launches()
         F.fp8z1_step_fused(L, F.make_hp(**hp), grad_shard=None if grad_rows else gf,
                            d_grad_params=F.param_pointers(g) if grad_rows else None, master_shard=p_,
                            m_shard=m_, v_shard=v_, fp8_shard=fq, d_fp8_params=F.param_pointers(f8),
                            scale_shard=sc, b0=b0, b1=b1, d_sumsq=s, d_found_inf=f)
+        # padded blocks before the full run, the run, padded blocks after it
+        assert F.fp8z1_kernel_launches() - n0 == {"whole": 3, "inside_full_run": 1, "across_runs": 3}[cut]
         torch.cuda.synchronize()
         for got, want in ((p_, op), (m_, om), (v_, ov), (sc, oscale)):
             assert np.array_equal(to_host(got).view(np.uint32), want.view(np.uint32))
