@@ -20,6 +20,7 @@ dp_size > 1 the other ranks' norm partials come through ``norm_hook``.
 from __future__ import annotations
 
 import ctypes as C
+import json
 from collections import OrderedDict
 from typing import Callable, List, Optional, Sequence
 
@@ -317,14 +318,29 @@ class ShardOptimizer:
         """Numbers for logging the last step (reads two device scalars): the
         global grad norm and clip coefficient (on this shard's sum of squares,
         after any norm hook), the loss scale the step used (pass it when the
-        scaler has moved since), t and S now, and whether it was skipped."""
+        scaler has moved since), t and S now, whether it was skipped, and how
+        many of this shard's blocks have scale 1 (amax 0 -- an all-zero block
+        -- or exactly 448)."""
         self.finish_host_step()
         s = float(self.sumsq.item())
         found = int(self.found_inf.item())
         used = self.scaler.scale if loss_scale is None else loss_scale
         norm, coef = (float("nan"), float("nan")) if found else F.fp8z1_clip_coef(s, self.hp["max_norm"], used)
         return {"global_norm": norm, "clip_coef": coef, "clipped": bool(not found and coef < 1.0),
-                "skipped": bool(found), "loss_scale": self.scaler.scale, "step": self.scaler.step}
+                "skipped": bool(found), "loss_scale": self.scaler.scale, "step": self.scaler.step,
+                "unit_scale_blocks": int((self.scales == 1.0).sum().item())}
+
+    def log_step(self, out, step_ms: Optional[float] = None, **extra) -> dict:
+        """Write ``stats()`` (plus the step time, the elements per second of
+        this shard, and any ``extra`` keys) as one JSON line to the text file
+        ``out``; return the line's dict."""
+        line = self.stats()
+        if step_ms is not None:
+            line["step_ms"] = step_ms
+            line["elem_per_s"] = (self.b1 - self.b0) * F.BLOCK_ELEMS / (step_ms / 1e3)
+        line.update(extra)
+        out.write(json.dumps(line) + "\n")
+        return line
 
 
 class CapturedStep:

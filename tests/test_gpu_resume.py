@@ -3,6 +3,7 @@ on -- bit-identical to an uninterrupted run.  The state is the four 1-D block
 buffers plus t and S; the norm reduction is deterministic, so resuming
 reproduces every bit."""
 import io
+import json
 
 import numpy as np
 import pytest
@@ -143,3 +144,24 @@ def test_stats_report_the_step(lib):
     assert st["global_norm"] == pytest.approx(gn, rel=1e-12)
     assert st["clip_coef"] == pytest.approx(cc, rel=1e-12)
     assert st["clipped"] == ap and not st["skipped"] and st["step"] == 1
+    assert st["unit_scale_blocks"] == int((opt.scales == 1.0).sum())
+    buf = io.StringIO()
+    line = opt.log_step(buf, step_ms=0.5, note="x")
+    assert json.loads(buf.getvalue()) == line and line["note"] == "x"
+    assert line["elem_per_s"] == pytest.approx(opt.nblk * 16384 / 0.5e-3)
+
+
+def test_unit_scale_blocks_counts_zero_blocks(lib):
+    """A block whose masters, moments and grads are all zero stays zero and
+    takes scale 1 (the scale when amax = 0); stats() counts such blocks."""
+    w = synth.workload("tiny", shapes=[(4, 128, 128)], dp=1, rank=0, max_norm=1e30)
+    opt = _make(w, 0)
+    master = synth.make_state(w, "master", "cuda")
+    master[0][1].zero_()
+    master[0][3].zero_()
+    opt.init_state(master)
+    g = synth.make_grads(w, 1, "cuda")
+    g[0][1].zero_()
+    g[0][3].zero_()
+    assert opt.step(g) == 0
+    assert opt.stats()["unit_scale_blocks"] == 2
