@@ -576,7 +576,7 @@ def main():
     ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--bf16-fold", type=int, default=0,
                     help="also time N launches each of the bf16 fold and unfold of the weights")
     ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "
