@@ -165,8 +165,7 @@ def bench_ours(args, rank, world, dist):
     def stages(path):
         """The kernels of one step on ``path``, as (label, launch) pairs."""
         def norm_fused():
-            opt.sumsq.zero_()
-            opt.found_inf.zero_()
+            F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
             F.fp8z1_fold_norm(opt.layout, gptrs, None, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
 
         def step_fused():
@@ -180,8 +179,7 @@ def bench_ours(args, rank, world, dist):
             F.fp8z1_fold(opt.layout, gptrs, gbuf, 4, opt.b0, opt.b1)
 
         def norm():
-            opt.sumsq.zero_()
-            opt.found_inf.zero_()
+            F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
             F.fp8z1_grad_norm(opt.layout, gbuf, opt.b0, opt.b1, opt.sumsq, opt.found_inf)
 
         def step():
@@ -434,8 +432,7 @@ def bench_mx(args, rank, world, dist):
     skipped = 0
     for i in range(args.steps):
         ev["norm"][i][0].record(stream)
-        opt.sumsq.zero_()
-        opt.found_inf.zero_()
+        F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
         F.fp8z1_mx_grad_norm(opt.layout, grad, opt.g0, opt.g1, opt.sumsq, opt.found_inf)
         ev["norm"][i][1].record(stream)
         hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)

@@ -348,6 +348,19 @@ int64_t persistent_grid(const fp8z1_layout* L, int64_t n)
 
 }  // namespace
 
+extern "C" int fp8z1_norm_reset(double* d_sumsq, int32_t* d_found_inf, void* stream)
+{
+    if (!d_sumsq || !d_found_inf) return FP8Z1_EINVAL;
+    if (!fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4)) return FP8Z1_EALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(d_sumsq, 0, sizeof(double), s) != cudaSuccess ||
+        cudaMemsetAsync(d_found_inf, 0, sizeof(int32_t), s) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    return FP8Z1_OK;
+}
+
 extern "C" int fp8z1_grad_norm(const fp8z1_layout* L, const float* grad_shard, int64_t b0, int64_t b1,
                                double* d_sumsq, int32_t* d_found_inf, void* stream)
 {

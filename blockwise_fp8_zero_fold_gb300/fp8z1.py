@@ -103,6 +103,7 @@ _SIGS = {
     "fp8z1_clip_coef": (C.c_int, [C.c_double, C.c_float, C.c_float, C.POINTER(C.c_double),
                                   C.POINTER(C.c_double)]),
     "fp8z1_kernel_launches": (C.c_int, [C.POINTER(C.c_uint64)]),
+    "fp8z1_norm_reset": (C.c_int, [_P, _P, _P]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
 
@@ -316,6 +317,11 @@ def fp8z1_step_scalars_from_hp(hp: fp8z1_adamw_hp, out=None) -> fp8z1_step_scala
     if out is not None:
         C.memmove(_ptr(out), C.addressof(sc), C.sizeof(sc))
     return sc
+
+
+def fp8z1_norm_reset(d_sumsq, d_found_inf, stream=None):
+    """*d_sumsq = 0, *d_found_inf = 0 (two memsets on ``stream``)."""
+    _check(lib().fp8z1_norm_reset(_ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)), "fp8z1_norm_reset")
 
 
 def fp8z1_kernel_launches() -> int:

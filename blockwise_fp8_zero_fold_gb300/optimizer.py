@@ -143,8 +143,7 @@ class ShardOptimizer:
         """Enqueue one step (no host synchronisation)."""
         if self._host_pending is not None:
             raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
-        self.sumsq.zero_()
-        self.found_inf.zero_()
+        F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
         if self.fused:
             gptrs = self._ptrs(grads)
@@ -240,8 +239,7 @@ class ShardOptimizer:
         prev = self._host_pending  # the step still in flight, if any
         comp = torch.cuda.current_stream(self.device)
         gptrs, fptrs = self._ptrs(grads), self._ptrs(fp8_params)
-        self.sumsq.zero_()  # after the previous step's update on this stream
-        self.found_inf.zero_()
+        F.fp8z1_norm_reset(self.sumsq, self.found_inf, comp)  # after the previous step's update
         for c, (p, e, r0, r1, k0, k1) in enumerate(chunks):  # grads in, norm as each chunk lands
             with torch.cuda.stream(self._copy_in):
                 if prev is not None:
@@ -384,16 +382,14 @@ class CapturedStep:
             self._write(self._h[0])
             opt.found_inf.fill_(1)
             self._enqueue(self._h[0], norm_hook=False)
-            opt.sumsq.zero_()
-            opt.found_inf.zero_()
+            F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
         side.synchronize()
         torch.cuda.current_stream(opt.device).wait_stream(side)
         self.graphs = []
         for h in self._h:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, pool=pool, stream=side):  # nothing is allocated inside
-                opt.sumsq.zero_()
-                opt.found_inf.zero_()
+                F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
                 self._enqueue(h, norm_hook=True)
             self.graphs.append(g)
 
@@ -469,8 +465,7 @@ class MxShardOptimizer:
         return flat[self.g0 * F.MX_GROUP:self.g1 * F.MX_GROUP]
 
     def launch_step(self, grad_shard: torch.Tensor, stream=None):
-        self.sumsq.zero_()
-        self.found_inf.zero_()
+        F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         F.fp8z1_mx_grad_norm(self.layout, grad_shard, self.g0, self.g1, self.sumsq, self.found_inf,
                              stream)
         if self.norm_hook is not None:

@@ -178,6 +178,12 @@ int fp8z1_unfold(const fp8z1_layout* layout, const void* src_shard, void* const*
 int fp8z1_grad_norm(const fp8z1_layout* layout, const float* grad_shard, int64_t b0, int64_t b1,
                     double* d_sumsq, int32_t* d_found_inf, void* stream);
 
+/* Clear a norm accumulator pair before a step: *d_sumsq = 0.0 and
+ * *d_found_inf = 0, as two memsets enqueued on `stream` (no kernel; capturable).
+ * Pointers: device; d_sumsq 8-byte aligned, d_found_inf 4-byte aligned.
+ * Errors: EINVAL (null), EALIGN, ECUDA. */
+int fp8z1_norm_reset(double* d_sumsq, int32_t* d_found_inf, void* stream);
+
 /* ---- grad norm without any allocation ------------------------------------ */
 
 /* The pages have no counterpart to this call: it serves callers that cannot

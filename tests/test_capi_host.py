@@ -119,6 +119,9 @@ def test_argument_errors_enqueue_nothing():
                   F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, 0.0, 1),
                   F.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 0.0, 1024.0, 1)]:
         assert lib.fp8z1_step(L.handle, C.byref(badhp), p, p, p, p, p, p, 0, 3, p, p, None) == F.EINVAL
+    assert lib.fp8z1_norm_reset(None, p, None) == F.EINVAL
+    assert lib.fp8z1_norm_reset(p + 4, p, None) == F.EALIGN
+    assert lib.fp8z1_norm_reset(p, p + 2, None) == F.EALIGN
     d = np.zeros(16, np.float32).ctypes.data
     assert lib.fp8z1_step_fused_dev(L.handle, None, None, None, p, p, p, p, p, None, p, None, None, 0, 3, p, p,
                                     None) == F.EINVAL
