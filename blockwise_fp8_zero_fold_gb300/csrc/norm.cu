@@ -481,7 +481,7 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
 //
 // Some callers cannot call cudaMalloc at all: a framework whose caching
 // allocator already owns the device memory (a foreign cudaMalloc can fail, or
-// make the driver synchronise the device), or a step loop that must never
+// make the CUDA driver synchronise the device), or a step loop that must never
 // block on an allocation.  fp8z1_grad_norm takes its workspace from a layout,
 // which fp8z1_build_layout allocates.  This variant takes it from a file-scope
 // array instead, so it needs neither a layout nor any allocation.

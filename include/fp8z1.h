@@ -188,7 +188,7 @@ int fp8z1_norm_reset(double* d_sumsq, int32_t* d_found_inf, void* stream);
 
 /* The pages have no counterpart to this call: it serves callers that cannot
  * call cudaMalloc at all -- a framework whose caching allocator already owns
- * the device memory (a foreign cudaMalloc can fail or make the driver
+ * the device memory (a foreign cudaMalloc can fail or make the CUDA driver
  * synchronise the device), or a step loop that must never block on an
  * allocation.  It computes what fp8z1_grad_norm computes, for the
  * `n_blocks` blocks at `grad_shard` (pointing at block b0 of the grad buffer;

@@ -2,7 +2,7 @@
 (every routine, compiled into tests/sanitize/oracle_driver.c) and the host
 side of the C ABI (layout.cpp linked alone with
 tests/sanitize/layout_driver.cpp, host-only layouts).  A sanitizer report
-aborts the driver, failing the test."""
+aborts the test program, failing the test."""
 import os
 import subprocess
 
