@@ -122,6 +122,28 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def _workload(args, synth):
+    """The named workload, cut to its first --experts experts of each 3-D
+    param and/or its first --params params when asked (smaller cases)."""
+    w = synth.workload(args.workload, dp=1, rank=0)
+    shapes = w.shapes
+    if args.experts:
+        shapes = [(min(e, args.experts), r, c) for e, r, c in shapes]
+    if args.params:
+        shapes = shapes[:args.params]
+    return w if shapes == w.shapes else synth.workload(args.workload, dp=1, rank=0, shapes=shapes)
+
+
+def _workload_label(args, shapes) -> str:
+    cut = "".join([f"[{args.experts} experts]" if args.experts else "",
+                   f"[first {args.params} params]" if args.params else ""])
+    if len(shapes) <= 8:
+        body = " + ".join(f"{e}x[{r},{c}]" for e, r, c in shapes)
+    else:
+        body = f"{len(shapes)} params, " + " + ".join(f"{e}x[{r},{c}]" for e, r, c in shapes[:3]) + " + ..."
+    return f"{args.workload}{cut}: {body}"
+
+
 def bench_ours(args, rank, world, dist):
     import torch
 
@@ -139,10 +161,7 @@ def bench_ours(args, rank, world, dist):
         dist.barrier()
     F.lib()
 
-    w = synth.workload(args.workload, dp=1, rank=0)
-    if args.experts:
-        w = synth.workload(args.workload, dp=1, rank=0,
-                           shapes=[(min(e, args.experts), r, c) for e, r, c in w.shapes])
+    w = _workload(args, synth)
     dp, shard_rank = (int(x) for x in args.shard.split(":")) if args.shard else (1, 0)
     opt = ShardOptimizer(w.shapes, dp_size=dp, rank=shard_rank, device=dev, loss_scale=w.loss_scale,
                          growth_interval=w.growth_interval,
@@ -267,7 +286,7 @@ def bench_ours(args, rank, world, dist):
     tr = _ncu_traffic()
     traffic = None
     if tr and tr.get("workload") == args.workload and tr.get("path") == args.path and \
-            tr.get("source_sha") == _step_source_sha() and not args.experts and whole:
+            tr.get("source_sha") == _step_source_sha() and not args.experts and not args.params and whole:
         traffic = tr.get("bytes_per_launch")
 
     # bf16 fold / unfold of the weights over the shard (2-byte elements)
@@ -346,7 +365,7 @@ def bench_ours(args, rank, world, dist):
         "dtype": "f32",
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
         "config": {
-            "workload": f"{args.workload}{'' if not args.experts else f'[{args.experts} experts]'}: " + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
+            "workload": _workload_label(args, w.shapes),
             "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "dp": "whole buffer (1 rank)" if whole else
                   f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1}) (this rank's norm partial; no all-reduce on one GPU)",
             "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -392,10 +411,7 @@ def bench_mx(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     F.lib()
-    w = synth.workload(args.workload, dp=1, rank=0)
-    if args.experts:
-        w = synth.workload(args.workload, dp=1, rank=0,
-                           shapes=[(min(e, args.experts), r, c) for e, r, c in w.shapes])
+    w = _workload(args, synth)
     opt = MxShardOptimizer(w.shapes, device=dev, loss_scale=w.loss_scale,
                            growth_interval=w.growth_interval,
                            **{k: v for k, v in w.hp().items() if k != "loss_scale"})
@@ -458,8 +474,7 @@ def bench_mx(args, rank, world, dist):
         "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
-        "config": {"workload": f"{args.workload} in the MXFP8 layout (E8M0 scale per 32 elements): "
-                               + " + ".join(f"{e}x[{r},{c}]" for e, r, c in w.shapes),
+        "config": {"workload": _workload_label(args, w.shapes) + " in the MXFP8 layout (E8M0 scale per 32 elements)",
                    "elems": n, "groups": opt.n_groups, "dp": "whole buffer (1 rank)",
                    "l2": "inputs larger than L2, no flush"},
         "scheme": "mx", "gpu_launches": launches, "kernels_ms": kern,
@@ -573,6 +588,8 @@ def main():
     ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
+    ap.add_argument("--params", type=int, default=0,
+                    help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--bf16-fold", type=int, default=0,
                     help="also time N launches each of the bf16 fold and unfold of the weights")

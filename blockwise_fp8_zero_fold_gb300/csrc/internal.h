@@ -86,6 +86,18 @@ struct NvtxRange {
     NvtxRange& operator=(const NvtxRange&) = delete;
 };
 
+// The pieces a grad norm without store reads for blocks [b0, b1), in order:
+// block ranges through the block table (partial row-block strips of a cut
+// param), runs of params the range holds whole, and contiguous element spans
+// of the whole strips of a cut param.  Together they cover every real grad
+// element of the range exactly once.
+struct NormPiece {
+    enum Kind { kBlocks, kWholeParams, kSpan } kind;
+    int64_t a, b;   // blocks [a, b) | params [a, b) | elements [a, b) of `param`
+    int32_t param;  // kSpan
+};
+void norm_pieces(const fp8z1_layout* L, int64_t b0, int64_t b1, std::vector<NormPiece>& out);
+
 // Kernels this library has enqueued in this process (every device and stream),
 // read through fp8z1_kernel_launches.
 std::atomic<uint64_t>& launch_counter();

@@ -166,6 +166,45 @@ extern "C" int fp8z1_build_layout(const fp8z1_shape* shapes, int32_t n_params, i
     return FP8Z1_OK;
 }
 
+void fp8z1::norm_pieces(const fp8z1_layout* L, int64_t b0, int64_t b1, std::vector<NormPiece>& out)
+{
+    out.clear();
+    auto add_blocks = [&](int64_t k0, int64_t k1) {
+        if (k0 == k1) return;
+        if (!out.empty() && out.back().kind == NormPiece::kBlocks && out.back().b == k0)
+            out.back().b = k1;  // adjacent block ranges: one launch
+        else
+            out.push_back({NormPiece::kBlocks, k0, k1, 0});
+    };
+    const std::vector<int64_t>& pb = L->param_block0;
+    int64_t p = std::upper_bound(pb.begin(), pb.end(), b0) - pb.begin() - 1;  // the param holding block b0
+    for (; b0 < b1 && p < L->n_params && pb[(size_t)p] < b1; ++p) {
+        const int64_t k0 = std::max(pb[(size_t)p], b0), k1 = std::min(pb[(size_t)p + 1], b1);
+        if (k0 == pb[(size_t)p] && k1 == pb[(size_t)p + 1]) {  // held whole
+            if (!out.empty() && out.back().kind == NormPiece::kWholeParams && out.back().b == p)
+                out.back().b = p + 1;
+            else
+                out.push_back({NormPiece::kWholeParams, p, p + 1, 0});
+            continue;
+        }
+        const fp8z1_shape sh = L->shapes[(size_t)p];
+        const int64_t rbs = tiles(sh.R), cbs = tiles(sh.C);
+        const int64_t l0 = k0 - pb[(size_t)p], l1 = k1 - pb[(size_t)p];
+        const int64_t s0 = (l0 + cbs - 1) / cbs, s1 = l1 / cbs;  // the whole strips [s0, s1)
+        if (s0 >= s1) {
+            add_blocks(k0, k1);
+            continue;
+        }
+        // strip s = e * rbs + rb starts at row e * R + 128 rb; strip E * rbs ends the param
+        auto strip_elem = [&](int64_t st) {
+            return st == sh.E * rbs ? sh.E * sh.R * sh.C : ((st / rbs) * sh.R + (st % rbs) * kTile) * sh.C;
+        };
+        add_blocks(k0, pb[(size_t)p] + s0 * cbs);
+        out.push_back({NormPiece::kSpan, strip_elem(s0), strip_elem(s1), (int32_t)p});
+        add_blocks(pb[(size_t)p] + s1 * cbs, k1);
+    }
+}
+
 std::atomic<uint64_t>& fp8z1::launch_counter()
 {
     static std::atomic<uint64_t> n{0};

@@ -109,18 +109,21 @@ __device__ __forceinline__ void sum_block(const float4 (&x)[kVec], double& acc, 
 }
 
 // Where the grads of one unit of work come from: the folded shard, a block of
-// the row-major params (through the block table), or a run of at most 16384
-// consecutive elements of one row-major param (a param the range holds whole:
-// its sum of squares needs no block structure).
-enum Src { kFolded, kRows, kParams };
+// the row-major params (through the block table), a run of at most 16384
+// consecutive elements of a param the range holds whole (from the layout's
+// run table), or a run of at most 16384 elements of one contiguous span of a
+// param (whole row-block strips of a param the range cuts: a strip is 128
+// full rows, and consecutive strips are consecutive in memory).  A sum of
+// squares needs no block structure, so only partial strips need the table.
+enum Src { kFolded, kRows, kParams, kSpan };
 
 // Where unit k's grads live in the row-major params.
 struct RowSrc {
     const float* tile;
     int64_t ld;
     int rows, cols;
-    int count;  // kParams: elements in the run
-    bool vec;   // 16-byte loads (kRows: ld % 4 == 0 and an aligned tile; kParams: an aligned run)
+    int count;  // kParams, kSpan: elements in the run
+    bool vec;   // 16-byte loads (kRows: ld % 4 == 0 and an aligned tile; kParams, kSpan: an aligned run)
     bool bad;   // null or misaligned param pointer
 };
 
@@ -152,11 +155,28 @@ __device__ __forceinline__ RowSrc param_src(const fp8z1_unit* __restrict__ units
     return s;
 }
 
+// Run k of a span: elements span_offset + 16384 k .. of param span_param.
+__device__ __forceinline__ RowSrc span_src(const float* const* __restrict__ params, int32_t param,
+                                           int64_t offset, int64_t elems, int64_t k)
+{
+    const float* base = params[param];
+    RowSrc s = {};
+    s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
+    const int64_t o = k * FP8Z1_BLOCK_ELEMS;
+    s.tile = s.bad ? nullptr : base + offset + o;
+    s.count = (int)(elems - o < FP8Z1_BLOCK_ELEMS ? elems - o : FP8Z1_BLOCK_ELEMS);
+    s.vec = !s.bad && (reinterpret_cast<uintptr_t>(s.tile) & 15) == 0;
+    return s;
+}
+
 struct NormArgs {
     const float4* g;              // folded grads at block b0 (kFolded)
     const fp8z1_block* lut;       // kRows
     const fp8z1_unit* units;      // kParams
-    const float* const* params;   // kRows, kParams: row-major FP32 grads
+    const float* const* params;   // kRows, kParams, kSpan: row-major FP32 grads
+    int64_t span_offset;          // kSpan: first element of the span in its param ...
+    int64_t span_elems;           // ... its length ...
+    int32_t span_param;           // ... and the param
     float4* store;                // STORE: folded grads at block b0
     int64_t b0;                   // first block (kRows: LUT index) or unit (kParams)
     int64_t nblocks;              // blocks of 16384, the last one possibly partial
@@ -188,7 +208,7 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
         }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
-    } else if constexpr (SRC == kParams) {
+    } else if constexpr (SRC == kParams || SRC == kSpan) {
         if (s.vec && s.count == FP8Z1_BLOCK_ELEMS) {  // a whole, aligned run
             const float4* p = reinterpret_cast<const float4*>(s.tile) + tid;
 #pragma unroll
@@ -247,6 +267,7 @@ __device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t k)
 {
     if (SRC == kRows) return row_src(a.lut, a.params, a.b0 + k);
     if (SRC == kParams) return param_src(a.units, a.params, a.b0 + k);
+    if (SRC == kSpan) return span_src(a.params, a.span_param, a.span_offset, a.span_elems, k);
     return RowSrc{};
 }
 
@@ -423,23 +444,41 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
             norm_kernel<kRows, false><<<grid, kThreads, 0, s>>>(a);
         }
     };
-    // Without the store, the params the range holds whole are read as flat
-    // runs of their row-major elements (a sum of squares needs no blocks);
-    // the cut params at either end go through the block table.  The pieces
-    // are separate launches on one stream, each adding its total to *d_sumsq.
-    const std::vector<int64_t>& pb = L->param_block0;
-    const int64_t pa = std::lower_bound(pb.begin(), pb.end(), b0) - pb.begin();        // first whole param
-    const int64_t pz = std::upper_bound(pb.begin(), pb.end(), b1) - pb.begin() - 1;    // one past the last
-    if (grad_shard || pa >= pz) {
+    // Without the store, the sum of squares needs no blocks: params the range
+    // holds whole are read as flat runs (the layout's run table), and the
+    // whole row-block strips of a param it cuts as one contiguous span; only
+    // the partial strips at either end go through the block table
+    // (fp8z1::norm_pieces).  The pieces are separate launches on one stream,
+    // each adding its total to *d_sumsq, in a fixed order: the sum is
+    // deterministic for a range.
+    if (grad_shard) {
         blocks(b0, b1);
-    } else {
-        blocks(b0, pb[(size_t)pa]);
-        const int64_t u0 = L->param_unit0[(size_t)pa], u1 = L->param_unit0[(size_t)pz];
-        a.b0 = u0;
-        a.nblocks = u1 - u0;
-        fp8z1::count_launch();
-        norm_kernel<kParams, false><<<(unsigned)persistent_grid(L, u1 - u0), kThreads, 0, s>>>(a);
-        blocks(pb[(size_t)pz], b1);
+        return fp8z1::launch_status();
+    }
+    std::vector<fp8z1::NormPiece> pieces;
+    try {
+        fp8z1::norm_pieces(L, b0, b1, pieces);
+    } catch (...) {
+        return FP8Z1_ENOMEM;
+    }
+    for (const fp8z1::NormPiece& pc : pieces) {
+        if (pc.kind == fp8z1::NormPiece::kBlocks) {
+            blocks(pc.a, pc.b);
+        } else if (pc.kind == fp8z1::NormPiece::kWholeParams) {
+            const int64_t u0 = L->param_unit0[(size_t)pc.a], u1 = L->param_unit0[(size_t)pc.b];
+            a.b0 = u0;
+            a.nblocks = u1 - u0;
+            fp8z1::count_launch();
+            norm_kernel<kParams, false><<<(unsigned)persistent_grid(L, u1 - u0), kThreads, 0, s>>>(a);
+        } else {
+            a.b0 = 0;
+            a.span_param = pc.param;
+            a.span_offset = pc.a;
+            a.span_elems = pc.b - pc.a;
+            a.nblocks = (pc.b - pc.a + FP8Z1_BLOCK_ELEMS - 1) / FP8Z1_BLOCK_ELEMS;
+            fp8z1::count_launch();
+            norm_kernel<kSpan, false><<<(unsigned)persistent_grid(L, a.nblocks), kThreads, 0, s>>>(a);
+        }
     }
     return fp8z1::launch_status();
 }

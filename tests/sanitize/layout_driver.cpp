@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "fp8z1.h"
+#include "internal.h"
 
 #define EXPECT(c)                                                     \
     do {                                                              \
@@ -85,6 +86,56 @@ int main()
     EXPECT(fp8z1_mx_destroy_layout(M) == FP8Z1_OK);
     const fp8z1_shape mx_bad = {1, 4, 33};
     EXPECT(fp8z1_mx_build_layout(&mx_bad, 1, 1, FP8Z1_LAYOUT_HOST_ONLY, &M) == FP8Z1_EINVAL);
+
+    // the pieces of a grad norm without store: for every sub-range [b0, b1),
+    // every real element of its blocks exactly once, nothing else
+    const std::vector<std::vector<fp8z1_shape>> small = {
+        {{1, 300, 200}},
+        {{3, 129, 257}, {1, 1, 1}, {2, 128, 128}, {1, 17, 690}},
+        {{2, 300, 260}, {1, 200, 131}, {2, 256, 256}},
+    };
+    std::vector<fp8z1::NormPiece> pieces;
+    for (const auto& shapes : small) {
+        const int32_t n = (int32_t)shapes.size();
+        fp8z1_layout* L = nullptr;
+        EXPECT(fp8z1_build_layout(shapes.data(), n, 1, FP8Z1_LAYOUT_HOST_ONLY, &L) == FP8Z1_OK);
+        const int64_t nblk = L->n_blocks;
+        std::vector<std::vector<uint8_t>> got(shapes.size()), want(shapes.size());
+        for (int64_t b0 = 0; b0 <= nblk; ++b0)
+            for (int64_t b1 = b0; b1 <= nblk; ++b1) {
+                for (int32_t i = 0; i < n; ++i) {
+                    const size_t ne = (size_t)(shapes[i].E * shapes[i].R * shapes[i].C);
+                    got[i].assign(ne, 0);
+                    want[i].assign(ne, 0);
+                }
+                auto mark_block = [&](std::vector<std::vector<uint8_t>>& cov, int64_t k) {
+                    const fp8z1_block& blk = L->lut[(size_t)k];
+                    for (int r = 0; r < blk.rows_real; ++r)
+                        for (int c = 0; c < blk.cols_real; ++c)
+                            ++cov[blk.param][(size_t)(blk.src_offset + (int64_t)r * blk.ld + c)];
+                };
+                for (int64_t k = b0; k < b1; ++k) mark_block(want, k);
+                fp8z1::norm_pieces(L, b0, b1, pieces);
+                for (const auto& pc : pieces) {
+                    if (pc.kind == fp8z1::NormPiece::kBlocks) {
+                        EXPECT(pc.a < pc.b);
+                        for (int64_t k = pc.a; k < pc.b; ++k) mark_block(got, k);
+                    } else if (pc.kind == fp8z1::NormPiece::kWholeParams) {
+                        EXPECT(pc.a < pc.b);
+                        for (int64_t q = pc.a; q < pc.b; ++q)
+                            for (auto& x : got[(size_t)q]) ++x;
+                    } else {
+                        EXPECT(pc.a < pc.b && pc.b <= (int64_t)got[(size_t)pc.param].size());
+                        for (int64_t e = pc.a; e < pc.b; ++e) ++got[(size_t)pc.param][(size_t)e];
+                    }
+                }
+                EXPECT(got == want);
+                for (const auto& v : got)
+                    for (uint8_t x : v) EXPECT(x <= 1);
+                EXPECT(pieces.size() <= 4 || b1 - b0 > 2);
+            }
+        EXPECT(fp8z1_destroy_layout(L) == FP8Z1_OK);
+    }
 
     uint64_t launches = 1;
     EXPECT(fp8z1_kernel_launches(&launches) == FP8Z1_OK && launches == 0);
