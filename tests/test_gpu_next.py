@@ -193,3 +193,36 @@ def test_mx_moe_full_size_sampled(lib):
             assert int(sc[int(pick[i])].item()) == int(osc[0])
         for buf, st in zip((master, mm, vv), state):
             assert np.array_equal(to_host(buf.view(-1, 32)[idx]).view(np.uint32), st.view(np.uint32))
+
+
+def test_mx_optimizer_steps_and_scaler(lib):
+    """MxShardOptimizer over four steps, the third with an inf (skipped: S
+    halves, t stays; growth every 2 clean steps), against the oracle's MX
+    step and loss scaler ("DeepSpeed ZeRO 优化" §六)."""
+    from blockwise_fp8_zero_fold_gb300.optimizer import MxShardOptimizer
+    shapes = [(2, 64, 96), (1, 100, 160)]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.5)
+    opt = MxShardOptimizer(shapes, loss_scale=1024.0, growth_interval=2, **hp)
+    n = sum(e * r * c for e, r, c in shapes)
+    assert opt.master.numel() == n
+    rng = np.random.default_rng(91)
+    p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    opt.master.copy_(torch.from_numpy(p))
+    op, om, ov = p.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    sc = oracle.Scaler(1024.0, 2)
+    for t in range(1, 5):
+        gh = (rng.standard_normal(n) * sc.scale * 1e-3).astype(np.float32)
+        if t == 3:
+            gh[n // 2] = np.inf
+        found = opt.step(torch.from_numpy(gh).cuda())
+        s, fi = oracle.sumsq(gh)
+        q, scl, skipped = oracle.mx_step(oracle.make_hp(loss_scale=sc.scale, step=sc.step + 1, **hp), s, fi,
+                                         gh, op, om, ov)
+        sc.update(int(fi))
+        assert found == fi == (1 if t == 3 else 0) and skipped == bool(fi)
+        assert (opt.scaler.scale, opt.scaler.step) == (sc.scale, sc.step)
+        for a, b in ((opt.master, op), (opt.m, om), (opt.v, ov)):
+            assert np.array_equal(to_host(a).view(np.uint32), b.view(np.uint32))
+        if not skipped:
+            assert np.array_equal(to_host(opt.codes), q) and np.array_equal(to_host(opt.scales), scl)
+    assert sc.step == 3 and sc.scale == 1024.0  # x2 after steps 1-2, /2 at the inf
