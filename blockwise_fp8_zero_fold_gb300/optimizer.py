@@ -371,7 +371,6 @@ class CapturedStep:
         nsc = C.sizeof(F.fp8z1_step_scalars) // 4
         self._h = [torch.zeros(nsc, dtype=torch.float32, pin_memory=True) for _ in range(slots)]
         self._d = torch.zeros(nsc, dtype=torch.float32, device=opt.device)
-        self._hp_struct = F.make_hp(step=1, loss_scale=1.0, **opt.hp)
         self._done = [torch.cuda.Event() for _ in range(slots)]
         self._next = 0
         # load every kernel once outside the capture: found_inf preset makes
@@ -394,10 +393,10 @@ class CapturedStep:
             self.graphs.append(g)
 
     def _write(self, h: torch.Tensor):
-        o, hp = self.opt, self._hp_struct
-        hp.step = o.scaler.step + 1
-        hp.loss_scale = o.scaler.scale
-        F.fp8z1_step_scalars_from_hp(hp, h)
+        """This step's scalars into pinned slot ``h``: t and S from the scaler,
+        the rest from ``opt.hp`` as it is now (a schedule may change lr)."""
+        o = self.opt
+        F.fp8z1_step_scalars_from_hp(F.make_hp(step=o.scaler.step + 1, loss_scale=o.scaler.scale, **o.hp), h)
 
     def _enqueue(self, h, norm_hook: bool):
         o = self.opt

@@ -112,7 +112,8 @@ def _oracle_steps(gsteps, ph, loss_scale0, growth):
         og = oracle.fold(SHAPES, gh)
         ss, fi = oracle.sumsq(og)
         if not fi:
-            hp = oracle.make_hp(loss_scale=sc.scale, step=sc.step + 1, **HP)
+            hp = oracle.make_hp(loss_scale=sc.scale, step=sc.step + 1,
+                                **dict(HP, lr=HP["lr"] / 2 if len(found) == 3 else HP["lr"]))
             q, scales, _ = oracle.step(hp, ss, fi, og, op, om, ov)
         found.append(int(fi))
         sc.update(int(fi))
@@ -121,8 +122,9 @@ def _oracle_steps(gsteps, ph, loss_scale0, growth):
 
 def test_captured_steps_match_oracle(lib):
     """Four steps through one captured graph, the third with a nan grad (a
-    skipped step: S halves, t stays): master, m, v, scales and the row-major
-    codes match the oracle's run of the same steps, and the eager path."""
+    skipped step: S halves, t stays) and the learning rate halved before the
+    fourth: master, m, v, scales and the row-major codes match the oracle's
+    run of the same steps, and the eager path."""
     rng = np.random.default_rng(11)
     ph = _rows(rng, 0.02)
     scale0, growth = 1024.0, 2
@@ -148,7 +150,9 @@ def test_captured_steps_match_oracle(lib):
         fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in SHAPES]
         cap = opt.capture(grads, fp8) if mode == "graph" else None
         got = []
-        for gh in scaled:
+        for k, gh in enumerate(scaled):
+            if k == 3:
+                opt.hp["lr"] = HP["lr"] / 2  # a schedule step: the graph must follow it
             for t, x in zip(grads, gh):
                 t.copy_(torch.from_numpy(x))
             got.append(cap.step() if cap else opt.step(grads, fp8))
