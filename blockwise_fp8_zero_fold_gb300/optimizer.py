@@ -481,3 +481,36 @@ class MxShardOptimizer:
     def step(self, grad_shard: torch.Tensor, stream=None) -> int:
         self.launch_step(grad_shard, stream)
         return self.finish_step()
+
+    # -- checkpoint / resume and logging, as ShardOptimizer's ------------------
+    def state_dict(self) -> dict:
+        return {
+            "shapes": [tuple(s) for s in self.shapes], "g0": self.g0, "g1": self.g1,
+            "master": self.master.cpu(), "m": self.m.cpu(), "v": self.v.cpu(),
+            "codes": self.codes.cpu(), "scales": self.scales.cpu(), "hp": dict(self.hp),
+            "scaler": {"scale": self.scaler.scale, "step": self.scaler.step,
+                       "good_steps": self.scaler.good_steps,
+                       "growth_interval": self.scaler.growth_interval},
+        }
+
+    def load_state_dict(self, sd: dict):
+        if [tuple(s) for s in sd["shapes"]] != [tuple(s) for s in self.shapes] or \
+                (sd["g0"], sd["g1"]) != (self.g0, self.g1):
+            raise ValueError("checkpoint was taken for another layout or shard")
+        for name in ("master", "m", "v", "codes", "scales"):
+            getattr(self, name).copy_(sd[name])
+        self.hp = dict(sd["hp"])
+        sc = sd["scaler"]
+        self.scaler = F.fp8z1_loss_scaler(sc["scale"], sc["step"], sc["good_steps"],
+                                          sc["growth_interval"])
+
+    def stats(self, loss_scale: Optional[float] = None) -> dict:
+        """The last step's global norm, clip coefficient, skip, t and S, and how
+        many of this shard's groups have scale 1 (E8M0 code 127)."""
+        s = float(self.sumsq.item())
+        found = int(self.found_inf.item())
+        used = self.scaler.scale if loss_scale is None else loss_scale
+        norm, coef = (float("nan"), float("nan")) if found else F.fp8z1_clip_coef(s, self.hp["max_norm"], used)
+        return {"global_norm": norm, "clip_coef": coef, "clipped": bool(not found and coef < 1.0),
+                "skipped": bool(found), "loss_scale": self.scaler.scale, "step": self.scaler.step,
+                "unit_scale_groups": int((self.scales == 127).sum().item())}

@@ -226,3 +226,45 @@ def test_mx_optimizer_steps_and_scaler(lib):
         if not skipped:
             assert np.array_equal(to_host(opt.codes), q) and np.array_equal(to_host(opt.scales), scl)
     assert sc.step == 3 and sc.scale == 1024.0  # x2 after steps 1-2, /2 at the inf
+
+
+def test_mx_optimizer_resume_is_bit_identical(lib):
+    """Checkpoint after two MX steps, reload into a fresh optimizer, carry on:
+    state, codes, scales and scaler equal an uninterrupted run."""
+    import io
+
+    from blockwise_fp8_zero_fold_gb300.optimizer import MxShardOptimizer
+    shapes = [(2, 64, 96), (1, 100, 160)]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.5)
+    n = sum(e * r * c for e, r, c in shapes)
+    rng = np.random.default_rng(5)
+    p = torch.from_numpy((rng.standard_normal(n) * 0.02).astype(np.float32))
+    grads = [torch.from_numpy((rng.standard_normal(n) * 1.0).astype(np.float32)).cuda() for _ in range(5)]
+    grads[2][n - 5] = float("nan")  # in rank 1's range
+
+    def fresh():
+        o = MxShardOptimizer(shapes, dp_size=2, rank=1, loss_scale=1024.0, growth_interval=2, **hp)
+        o.master.copy_(o.shard_of(p.cuda()))
+        return o
+
+    ref = fresh()
+    for g in grads:
+        ref.step(ref.shard_of(g))
+    first = fresh()
+    for g in grads[:2]:
+        first.step(first.shard_of(g))
+    buf = io.BytesIO()
+    torch.save(first.state_dict(), buf)
+    buf.seek(0)
+    second = MxShardOptimizer(shapes, dp_size=2, rank=1, loss_scale=1.0, growth_interval=2, **hp)
+    second.load_state_dict(torch.load(buf))
+    for g in grads[2:]:
+        second.step(second.shard_of(g))
+    for name in ("master", "m", "v", "codes", "scales"):
+        assert torch.equal(getattr(ref, name).view(torch.uint8), getattr(second, name).view(torch.uint8)), name
+    assert (ref.scaler.scale, ref.scaler.step) == (second.scaler.scale, second.scaler.step)
+    st = second.stats()
+    assert not st["skipped"] and st["step"] == ref.scaler.step == 4
+    assert st["unit_scale_groups"] == int((second.scales == 127).sum())
+    with pytest.raises(ValueError):
+        MxShardOptimizer(shapes, dp_size=2, rank=0, **hp).load_state_dict(ref.state_dict())
