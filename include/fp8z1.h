@@ -246,10 +246,16 @@ int fp8z1_step(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const float
  * read them the same way.  `d_grad_params`: DEVICE array of n_params DEVICE
  * pointers to FP32 row-major params (4-byte aligned).  A null or misaligned
  * entry sets FP8Z1_DEVSTATUS_BADPTR and *d_found_inf (so the step is skipped).
- * The same reduction as fp8z1_grad_norm: deterministic for a given device and
- * range, within about 1e-13 of the exact sum; it uses the same layout
- * workspace, so calls sharing a layout must not overlap on the device.
- * Errors: EINVAL, EALIGN, ENODEV, ECUDA. */
+ * Without the store the sum needs no block structure: the params the range
+ * holds whole, and the whole row-block strips of a param it cuts, are read as
+ * flat runs of their row-major elements; only partial strips go block by
+ * block.  The call then enqueues one launch per piece (whole params, a span,
+ * partial strips), each adding its total to *d_sumsq.  The result is
+ * deterministic for a given device and range, and within about 1e-13 of the
+ * exact sum (the summation order differs from fp8z1_grad_norm's, so the two
+ * agree to that, not bit for bit).  It uses the layout's norm workspace, so
+ * calls sharing a layout must not overlap on the device.
+ * Errors: EINVAL, EALIGN, ENODEV, ECUDA, ENOMEM. */
 int fp8z1_fold_norm(const fp8z1_layout* layout, const float* const* d_grad_params, float* grad_shard,
                     int64_t b0, int64_t b1, double* d_sumsq, int32_t* d_found_inf, void* stream);
 
