@@ -390,6 +390,7 @@ def bench_ours(args, rank, world, dist):
     }
     if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)
+        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.workload, args.cpu_sample_experts)
     return out
 
 
@@ -534,11 +535,65 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+    def run_threads(self, threads: int) -> float:
+        """The same pass with the oracle's calls on ``threads`` contiguous block
+        ranges at once (ctypes releases the GIL during each call; blocks are
+        independent once the global sum of squares is known)."""
+        from concurrent.futures import ThreadPoolExecutor
+
+        import numpy as np
+
+        import oracle
+
+        self.t += 1
+        nb = self.n_pad // 16384
+        cuts = [nb * i // threads for i in range(threads + 1)]
+        ranges = [(a, b) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+        g = np.empty(self.n_pad, np.float32)
+        q = np.empty(self.n_pad, np.uint8)
+        hp = oracle.make_hp(step=self.t, **self.w.hp())
+        E = 16384
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(len(ranges)) as ex:
+            def fold(r):
+                g[r[0] * E:r[1] * E] = oracle.fold(self.shapes, self.g_rows, r[0], r[1])
+            list(ex.map(fold, ranges))
+            s, f = oracle.sumsq_parallel([g], threads=len(ranges))
+
+            def step(r):
+                sl = slice(r[0] * E, r[1] * E)
+                q[sl] = oracle.step(hp, s, f, g[sl], self.p[sl], self.m[sl], self.v[sl])[0]
+            list(ex.map(step, ranges))
+            list(ex.map(lambda r: oracle.unfold(self.shapes, q[r[0] * E:r[1] * E], self.outs, r[0], r[1]),
+                        ranges))
+        return time.perf_counter() - t0
+
+
+def _host_info():
+    ram = None
+    try:
+        with open("/proc/meminfo") as f:
+            ram = round(int(f.readline().split()[1]) / 2**20, 1)
+    except Exception:
+        pass
+    return {"cpu": _cpu_name(), "host_cores": os.cpu_count(), "ram_gb": ram}
+
+
 def cpu_baseline(workload: str, experts: int):
     s = OracleSample(workload, experts)
     t = s.run()
     return {"value": s.n_pad / t, "unit": "elem/s", "cores": 1, "kind": "oracle",
-            "sample": s.sample, "seconds": t, "cpu": _cpu_name()}
+            "sample": s.sample, "seconds": t, **_host_info()}
+
+
+def cpu_baseline_all_cores(workload: str, experts: int):
+    """The oracle as it stands, on every host core (one thread per core, each
+    on a contiguous block range).  A second reported baseline."""
+    s = OracleSample(workload, experts)
+    n = os.cpu_count() or 1
+    t = s.run_threads(n)
+    return {"value": s.n_pad / t, "unit": "elem/s", "cores": n, "kind": "oracle, block ranges on every core",
+            "sample": s.sample, "seconds": t, **_host_info()}
 
 
 def _cpu_name():
@@ -568,7 +623,7 @@ def bench_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{args.workload} (oracle on a bounded sample: {smp.sample})"},
         "cpu_baseline": {"value": v, "unit": "elem/s", "cores": 1, "kind": "oracle",
-                         "sample": smp.sample, "cpu": _cpu_name()},
+                         "sample": smp.sample, **_host_info()},
         "e2e": {"value": v, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

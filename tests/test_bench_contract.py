@@ -77,3 +77,21 @@ def test_bench_line_shard_and_bf16_fold():
 def test_bench_line_mx():
     d = _run("--scheme", "mx", "--workload", "moe", "--experts", "1", "--steps", "3", "--warmup", "3")
     _check_ours(d, 3)
+
+
+def test_threaded_oracle_pass_equals_single_thread():
+    """The all-cores CPU baseline runs the same oracle calls on block ranges in
+    threads: its state and codes equal the single-thread pass's."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    one, many = bench.OracleSample("tiny", 1), bench.OracleSample("tiny", 1)
+    one.run()
+    many.run_threads(3)
+    for name in ("p", "m", "v"):
+        assert np.array_equal(getattr(one, name).view(np.uint32), getattr(many, name).view(np.uint32))
+    for a, b in zip(one.outs, many.outs):
+        assert np.array_equal(a, b)
+    d = bench.cpu_baseline_all_cores("tiny", 1)
+    assert d["cores"] == (os.cpu_count() or 1) and d["value"] > 0 and d["host_cores"] >= 1
