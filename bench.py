@@ -596,12 +596,17 @@ def cpu_baseline_all_cores(workload: str, experts: int):
             "sample": s.sample, "seconds": t, **_host_info()}
 
 
+_ARM_PARTS = {"0xd4f": "Arm Neoverse V2 (Grace)", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1"}
+
+
 def _cpu_name():
+    """The CPU model: 'model name' on x86, the Arm part number named where known."""
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 if line.lower().startswith(("model name", "cpu part")):
-                    return line.split(":", 1)[1].strip()
+                    v = line.split(":", 1)[1].strip()
+                    return _ARM_PARTS.get(v.lower(), v)
     except Exception:
         pass
     return os.uname().machine
