@@ -215,6 +215,13 @@ def bench_ours(args, rank, world, dist):
 
     def run_steps(path, k, events=None):
         skipped = 0
+        if path == "fused" and args.pipeline:
+            # each step enqueued before the previous one's found_inf is read:
+            # the kernel picks t and S by that flag, the host reads it a step late
+            for i in range(k):
+                ev = None if events is None else {"norm": events["fold_norm"][i], "step": events["step"][i]}
+                skipped += sum(opt.launch_step_async(grads, fp8, stream, ev))
+            return skipped + sum(opt.drain())
         for i in range(k):
             for name, fn in stages(path):
                 if events is not None:
@@ -286,6 +293,7 @@ def bench_ours(args, rank, world, dist):
     tr = _ncu_traffic()
     traffic = None
     if tr and tr.get("workload") == args.workload and tr.get("path") == args.path and \
+            bool(tr.get("pipelined")) == bool(args.pipeline and args.path == "fused") and \
             tr.get("source_sha") == _step_source_sha() and not args.experts and not args.params and whole:
         traffic = tr.get("bytes_per_launch")
 
@@ -374,13 +382,15 @@ def bench_ours(args, rank, world, dist):
         },
         "gpu_launches": launches,
         "path": args.path,
+        "pipelined": bool(args.pipeline and args.path == "fused"),
         "kernels_ms": kern,
         "kernels_gbs": gbs,
         "other_path": other,
         "step_kernel_elem_per_s": n_pad / (kern["step"] / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "fp8z1_step_fused" if args.path == "fused" else "fp8z1_step",
+                     "kernel": ("fp8z1_step_fused_select" if args.pipeline else "fp8z1_step_fused")
+                               if args.path == "fused" else "fp8z1_step",
                      "peak_source": peak_kind,
                      "bytes_per_launch": step_bytes},
         "clocks": clk,
@@ -648,6 +658,9 @@ def main():
     ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
+    ap.add_argument("--pipeline", type=int, default=1,
+                    help="fused path: enqueue each step before the previous one's found_inf is read "
+                         "(ShardOptimizer.launch_step_async)")
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)

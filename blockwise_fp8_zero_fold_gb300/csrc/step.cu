@@ -88,15 +88,19 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
 
 namespace {
 
-int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const StepScalars* h_scalars,
-                    StepScalars* d_scalars,
+int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const fp8z1_adamw_hp* hp_if_set,
+                    const int32_t* d_select, const StepScalars* h_scalars, StepScalars* d_scalars,
                     const float* grad_shard, const float* const* d_grad_params, float* master_shard,
                     float* m_shard, float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params,
                     float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0, int64_t b1,
                     const double* d_sumsq, const int32_t* d_found_inf, void* stream)
 {
-    // exactly one scalar source: hp by value, or d_scalars
+    // exactly one scalar source: hp by value (optionally a second set picked
+    // by *d_select), or d_scalars
     if ((hp == nullptr) == (d_scalars == nullptr)) return FP8Z1_EINVAL;
+    if ((hp_if_set == nullptr) != (d_select == nullptr)) return FP8Z1_EINVAL;
+    if (hp_if_set && (block_cos || !in_domain(hp_if_set))) return FP8Z1_EINVAL;
+    if (d_select && !fp8z1::aligned(d_select, 4)) return FP8Z1_EALIGN;
     int st = check_common(L, hp, master_shard, m_shard, v_shard, scale_shard, b0, b1, d_sumsq, d_found_inf);
     if (st != FP8Z1_OK) return st;
     if (d_scalars && !fp8z1::aligned(d_scalars, 4)) return FP8Z1_EALIGN;
@@ -128,7 +132,9 @@ int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const StepS
     a.block_underflow = block_underflow;
     a.status = L->d_status;
     a.dsc = d_scalars;
+    a.select = d_select;
     if (hp) a.c = scalars(hp);
+    if (hp_if_set) a.c2 = scalars(hp_if_set);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (h_scalars && cudaMemcpyAsync(d_scalars, h_scalars, sizeof(StepScalars),
                                      cudaMemcpyHostToDevice, s) != cudaSuccess) {
@@ -137,7 +143,7 @@ int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const StepS
     }
     const unsigned forms = (d_grad_params ? kGradRows : 0u) | (d_fp8_params ? kCodesRows : 0u) |
                            (fp8_shard ? kCodesFolded : 0u) | (block_cos ? kMonitors : 0u) |
-                           (d_scalars ? kDevScalars : 0u);
+                           (d_scalars ? kDevScalars : 0u) | (d_select ? kSelScalars : 0u);
     launch_segments(L, a, b0, b1, s, forms);
     return fp8z1::launch_status();
 }
@@ -153,9 +159,9 @@ extern "C" int fp8z1_step_fused(const fp8z1_layout* L, const fp8z1_adamw_hp* hp,
 {
     fp8z1::NvtxRange nvtx_range("fp8z1_step_fused");
     if (!hp) return FP8Z1_EINVAL;
-    return step_fused_impl(L, hp, nullptr, nullptr, grad_shard, d_grad_params, master_shard, m_shard, v_shard,
-                           fp8_shard, d_fp8_params, scale_shard, block_cos, block_underflow, b0, b1, d_sumsq,
-                           d_found_inf, stream);
+    return step_fused_impl(L, hp, nullptr, nullptr, nullptr, nullptr, grad_shard, d_grad_params, master_shard,
+                           m_shard, v_shard, fp8_shard, d_fp8_params, scale_shard, block_cos, block_underflow, b0,
+                           b1, d_sumsq, d_found_inf, stream);
 }
 
 extern "C" int fp8z1_step_fused_dev(const fp8z1_layout* L, const fp8z1_step_scalars* h_scalars,
@@ -167,9 +173,24 @@ extern "C" int fp8z1_step_fused_dev(const fp8z1_layout* L, const fp8z1_step_scal
 {
     fp8z1::NvtxRange nvtx_range("fp8z1_step_fused_dev");
     if (!d_scalars) return FP8Z1_EINVAL;
-    return step_fused_impl(L, nullptr, h_scalars, d_scalars, grad_shard, d_grad_params, master_shard, m_shard,
+    return step_fused_impl(L, nullptr, nullptr, nullptr, h_scalars, d_scalars, grad_shard, d_grad_params,
+                           master_shard, m_shard,
                            v_shard, fp8_shard, d_fp8_params, scale_shard, block_cos, block_underflow, b0, b1,
                            d_sumsq, d_found_inf, stream);
+}
+
+extern "C" int fp8z1_step_fused_select(const fp8z1_layout* L, const fp8z1_adamw_hp* hp_if_clear,
+                                       const fp8z1_adamw_hp* hp_if_set, const int32_t* d_select,
+                                       const float* grad_shard, const float* const* d_grad_params,
+                                       float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                                       uint8_t* const* d_fp8_params, float* scale_shard, int64_t b0, int64_t b1,
+                                       const double* d_sumsq, const int32_t* d_found_inf, void* stream)
+{
+    fp8z1::NvtxRange nvtx_range("fp8z1_step_fused_select");
+    if (!hp_if_clear || !hp_if_set || !d_select) return FP8Z1_EINVAL;
+    return step_fused_impl(L, hp_if_clear, hp_if_set, d_select, nullptr, nullptr, grad_shard, d_grad_params,
+                           master_shard, m_shard, v_shard, fp8_shard, d_fp8_params, scale_shard, nullptr, nullptr,
+                           b0, b1, d_sumsq, d_found_inf, stream);
 }
 
 extern "C" int fp8z1_step_scalars_from_hp(const fp8z1_adamw_hp* hp, fp8z1_step_scalars* out)

@@ -20,7 +20,11 @@ enum : unsigned {
     kCodesFolded = 4u,  // codes written to the folded code shard
     kMonitors = 8u,     // per-block underflow count and cosine
     kDevScalars = 16u,  // step scalars read from device memory
+    kSelScalars = 32u,  // two scalar sets by value, picked by a device flag
 };
+
+// where the kernel takes its step scalars from
+enum ScalarSource : int { kScValue = 0, kScDevice = 1, kScSelect = 2 };
 
 struct StepArgs {
     const float4* grad;          // folded grad shard (!kGradRows)
@@ -40,7 +44,9 @@ struct StepArgs {
     float* block_cos;            // kMonitors: cosine(master, dequantised) per block
     uint32_t* block_underflow;   // kMonitors: non-zero masters whose code is 0, per block
     const StepScalars* dsc;      // kDevScalars: the scalars in device memory
-    StepScalars c;               // otherwise: the scalars by value
+    const int32_t* select;       // kSelScalars: c when *select == 0, else c2
+    StepScalars c;               // the scalars by value
+    StepScalars c2;              // kSelScalars: the other set
 };
 
 // One launch of nb blocks from a.blk_off on; `forms` is an OR of the bits above.

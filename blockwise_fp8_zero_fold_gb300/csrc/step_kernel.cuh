@@ -142,17 +142,20 @@ __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScala
     }
 }
 
-template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, bool DEVSC, bool PAD>
+template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, int SC, bool PAD>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
     __shared__ StepScalars s_c;
+    __shared__ int s_alt;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        if (DEVSC) s_c = *a.dsc;
-        s_gscale = grad_factor(*a.sumsq, DEVSC ? s_c : a.c);
+        if (SC == kScDevice) s_c = *a.dsc;
+        const bool alt = SC == kScSelect && *a.select != 0;
+        s_alt = alt;
+        s_gscale = grad_factor(*a.sumsq, SC == kScDevice ? s_c : (alt ? a.c2 : a.c));
     }
 
     // the block's place in its row-major param and its real extent
@@ -192,12 +195,21 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     }
     __syncthreads();
     const float gs = s_gscale;
-    const StepScalars& c = DEVSC ? s_c : a.c;
 
     const int64_t base = kb * (FP8Z1_BLOCK_ELEMS / 4) + tid;
     float pn[4 * kVec];
     float amax = 0.0f;
-    update_chunks<GRAD_ROWS, PAD>(a, c, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+    if constexpr (SC == kScSelect) {
+        // one uniform branch, each side with its scalars as kernel-parameter
+        // operands (no registers held for them)
+        if (s_alt)
+            update_chunks<GRAD_ROWS, PAD>(a, a.c2, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+        else
+            update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+    } else {
+        update_chunks<GRAD_ROWS, PAD>(a, SC == kScDevice ? s_c : a.c, gs, base, tid, gtile, ld, rows, cols,
+                                      gvec, pn, amax);
+    }
 
     amax = warp_max(amax);
     if ((tid & 31) == 0) s_amax[tid >> 5] = amax;
@@ -274,18 +286,21 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
 {
     // the forms the entry points use: grads folded or row-major, codes to
     // the folded shard and/or row-major, with or without monitors, scalars by
-    // value or in device memory
-#define FP8Z1_STEP_FORM(GR, CR, CF, MON, DEV)                                                        \
+    // value, in device memory, or two sets by value picked by a device flag
+    // (without monitors)
+#define FP8Z1_STEP_FORM(GR, CR, CF, MON, SCAL)                                                       \
     if (forms == ((GR ? kGradRows : 0u) | (CR ? kCodesRows : 0u) | (CF ? kCodesFolded : 0u) |         \
-                  (MON ? kMonitors : 0u) | (DEV ? kDevScalars : 0u))) {                              \
-        step_kernel<GR, CR, CF, MON, DEV, PAD><<<(unsigned)nb, kThreads, 0, s>>>(a);                 \
+                  (MON ? kMonitors : 0u) | (SCAL == kScDevice ? kDevScalars : 0u) |                   \
+                  (SCAL == kScSelect ? kSelScalars : 0u))) {                                         \
+        step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, 0, s>>>(a);                \
         return;                                                                                      \
     }
 #define FP8Z1_STEP_FORMS_GC(GR, CR, CF)                                                              \
-    FP8Z1_STEP_FORM(GR, CR, CF, false, false)                                                        \
-    FP8Z1_STEP_FORM(GR, CR, CF, false, true)                                                         \
-    FP8Z1_STEP_FORM(GR, CR, CF, true, false)                                                         \
-    FP8Z1_STEP_FORM(GR, CR, CF, true, true)
+    FP8Z1_STEP_FORM(GR, CR, CF, false, kScValue)                                                     \
+    FP8Z1_STEP_FORM(GR, CR, CF, false, kScDevice)                                                    \
+    FP8Z1_STEP_FORM(GR, CR, CF, false, kScSelect)                                                    \
+    FP8Z1_STEP_FORM(GR, CR, CF, true, kScValue)                                                      \
+    FP8Z1_STEP_FORM(GR, CR, CF, true, kScDevice)
     FP8Z1_STEP_FORMS_GC(true, true, true)
     FP8Z1_STEP_FORMS_GC(true, true, false)
     FP8Z1_STEP_FORMS_GC(true, false, true)

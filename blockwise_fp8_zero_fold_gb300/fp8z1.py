@@ -88,6 +88,8 @@ _SIGS = {
                                    _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_step_fused_dev": (C.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                        C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_step_fused_select": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_adamw_hp), _P, _P, _P,
+                                          _P, _P, _P, _P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_step_scalars_from_hp": (C.c_int, [C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_step_scalars)]),
     "fp8z1_paramwise_split": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, _P, _P,
                                         C.POINTER(C.c_int64)]),
@@ -306,6 +308,19 @@ def fp8z1_step_fused_dev(layout: Layout, h_scalars, d_scalars, *, grad_shard=Non
                                       _ptr(block_cos), _ptr(block_underflow), int(b0), int(b1),
                                       _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_step_fused_dev")
+
+
+def fp8z1_step_fused_select(layout: Layout, hp_if_clear: fp8z1_adamw_hp, hp_if_set: fp8z1_adamw_hp,
+                            d_select, *, grad_shard=None, d_grad_params=None, master_shard, m_shard, v_shard,
+                            fp8_shard=None, d_fp8_params=None, scale_shard, b0: int, b1: int, d_sumsq,
+                            d_found_inf, stream=None):
+    """fp8z1_step_fused with ``hp_if_clear`` when *d_select == 0, else
+    ``hp_if_set``, picked on the device when the kernel runs."""
+    _check(lib().fp8z1_step_fused_select(layout.handle, C.byref(hp_if_clear), C.byref(hp_if_set), _ptr(d_select),
+                                         _ptr(grad_shard), _ptr(d_grad_params), _ptr(master_shard), _ptr(m_shard),
+                                         _ptr(v_shard), _ptr(fp8_shard), _ptr(d_fp8_params), _ptr(scale_shard),
+                                         int(b0), int(b1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
+           "fp8z1_step_fused_select")
 
 
 def fp8z1_step_scalars_from_hp(hp: fp8z1_adamw_hp, out=None) -> fp8z1_step_scalars:

@@ -58,6 +58,7 @@ class ShardOptimizer:
         self._ptr_cache: "OrderedDict[tuple, torch.Tensor]" = OrderedDict()
         self._host_pending: Optional[int] = None  # step_from_host(wait=False) in flight
         self._host_slot = 0
+        self._async = None  # launch_step_async state, made on first use
 
     # -- pointer arrays for fold/unfold ------------------------------------
     _PTR_CACHE = 16  # distinct tensor sets whose device pointer arrays are kept
@@ -143,6 +144,8 @@ class ShardOptimizer:
         """Enqueue one step (no host synchronisation)."""
         if self._host_pending is not None:
             raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
+        if self._async is not None and self._async["inflight"]:
+            raise RuntimeError("steps from launch_step_async are in flight: call drain() first")
         F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
         if self.fused:
@@ -212,6 +215,8 @@ class ShardOptimizer:
         ``finish_host_step``, which also waits for the copies back: the host
         FP8 weights and scales are complete only after it."""
         assert self.fused, "step_from_host runs the fused path"
+        if self._async is not None and self._async["inflight"]:
+            raise RuntimeError("steps from launch_step_async are in flight: call drain() first")
         if (self.b0, self.b1) != (0, self.nblk):
             raise ValueError("step_from_host needs the whole buffer as the shard (dp_size 1)")
         if grads is None:
@@ -295,6 +300,103 @@ class ShardOptimizer:
         found = self._retire_host_step(self._host_pending)
         self._host_pending = None
         return found
+
+    # -- steps enqueued ahead of their found_inf --------------------------------
+    def launch_step_async(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
+                          stream=None, events: Optional[dict] = None) -> List[int]:
+        """Enqueue one fused step without waiting for the previous one.
+
+        The method reads found_inf after every step to set the next step's t
+        and S ("DeepSpeed ZeRO 优化" §六).  Here the host reads it one step
+        late: while step k-1 may still run, step k is enqueued with both
+        candidate hyper-parameter sets (step k-1 clean: t+1 and S after growth;
+        skipped: t and S/2), and the kernel picks one by step k-1's found_inf
+        (fp8z1_step_fused_select).  Each step's norm accumulators alternate
+        between two slots, and its found_inf is copied to pinned memory right
+        after its norm; the host waits only for that copy of step k-2 before
+        enqueuing step k.  Results equal ``step`` run one at a time.
+
+        Returns the found_inf of the steps resolved by this call (oldest
+        first); ``drain`` resolves the rest.  ``events``: optional
+        {"norm": (start, end), "step": (start, end)} CUDA events to record
+        around the two kernels on ``stream``."""
+        if not self.fused:
+            raise ValueError("launch_step_async runs the fused path")
+        if self._host_pending is not None:
+            raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
+        st = self._async
+        if st is None:
+            st = self._async = {
+                "sumsq": torch.zeros(2, dtype=torch.float64, device=self.device),
+                "found": torch.zeros(2, dtype=torch.int32, device=self.device),
+                "flags": [torch.zeros(1, dtype=torch.int32, pin_memory=True) for _ in range(2)],
+                "done": [torch.cuda.Event() for _ in range(2)],
+                "k": 0, "inflight": [],  # slots of unresolved steps, oldest first
+            }
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        resolved = []
+        while len(st["inflight"]) >= 2:  # resolve step k-2: its flag copy ran long ago
+            resolved.append(self._resolve_async())
+        slot = st["k"] % 2
+        st["k"] += 1
+        sumsq, found = st["sumsq"][slot:slot + 1], st["found"][slot:slot + 1]
+        gptrs = self._ptrs(grads)
+        ev = events or {}
+        if "norm" in ev:
+            ev["norm"][0].record(s)
+        F.fp8z1_norm_reset(sumsq, found, s)
+        F.fp8z1_fold_norm(self.layout, gptrs, None, self.b0, self.b1, sumsq, found, s)
+        if self.norm_hook is not None:
+            with torch.cuda.stream(s):
+                self.norm_hook(sumsq, found)
+        if "norm" in ev:
+            ev["norm"][1].record(s)
+        with torch.cuda.stream(s):
+            st["flags"][slot].copy_(found, non_blocking=True)
+        st["done"][slot].record(s)
+        kw = dict(d_grad_params=gptrs, master_shard=self.master, m_shard=self.m, v_shard=self.v,
+                  fp8_shard=self.codes if fp8_params is None else None,
+                  d_fp8_params=None if fp8_params is None else self._ptrs(fp8_params),
+                  scale_shard=self.scales, b0=self.b0, b1=self.b1, d_sumsq=sumsq, d_found_inf=found, stream=s)
+        if "step" in ev:
+            ev["step"][0].record(s)
+        if not st["inflight"]:
+            F.fp8z1_step_fused(self.layout, self._hp_after(None), **kw)
+        else:
+            prev = st["inflight"][0]
+            F.fp8z1_step_fused_select(self.layout, self._hp_after(0), self._hp_after(1),
+                                      st["found"][prev:prev + 1], **kw)
+        if "step" in ev:
+            ev["step"][1].record(s)
+        st["inflight"].append(slot)
+        # the latest step's accumulators, for stats() once drained
+        self.sumsq, self.found_inf = sumsq, found
+        return resolved
+
+    def _hp_after(self, found_prev: Optional[int]):
+        """The hyper-parameters of the next step, given the resolved scaler and,
+        when one step is unresolved, its found_inf."""
+        sc = self.scaler
+        if found_prev is not None:
+            sc = F.fp8z1_loss_scaler(sc.scale, sc.step, sc.good_steps, sc.growth_interval)
+            F.fp8z1_scaler_update(sc, int(found_prev))
+        return F.make_hp(step=sc.step + 1, loss_scale=sc.scale, **self.hp)
+
+    def _resolve_async(self) -> int:
+        st = self._async
+        slot = st["inflight"].pop(0)
+        st["done"][slot].synchronize()
+        found = int(st["flags"][slot].item())
+        F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
+    def drain(self) -> List[int]:
+        """Wait for every step enqueued by ``launch_step_async`` and return
+        their found_inf, oldest first (the loss scaler and t then count them)."""
+        out = []
+        while self._async is not None and self._async["inflight"]:
+            out.append(self._resolve_async())
+        return out
 
     def finish_step(self) -> int:
         """Read found_inf (synchronises) and update the loss scale and t."""

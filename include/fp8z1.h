@@ -289,6 +289,26 @@ int fp8z1_step_fused(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const
                      float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0,
                      int64_t b1, const double* d_sumsq, const int32_t* d_found_inf, void* stream);
 
+/* ---- the step with two candidate hyper-parameter sets ------------------------ */
+
+/* fp8z1_step_fused (without monitors) taking two hyper-parameter sets, both by
+ * value: the kernel uses `hp_if_clear` when *d_select == 0 and `hp_if_set`
+ * otherwise, reading *d_select (device, 4-byte aligned) when it runs.  With
+ * d_select = the previous step's found_inf, a caller can enqueue a step
+ * before it knows whether the previous one was skipped ("DeepSpeed ZeRO 优化"
+ * §六): hp_if_clear holds t+1 and the loss scale after a clean step,
+ * hp_if_set the t and halved scale after a skipped one.  The host need not
+ * wait for each step to finish before enqueuing the next, and the results
+ * are those of fp8z1_step_fused with the set picked.  Both sets ride as kernel
+ * parameters, so the pick costs no registers.
+ * Errors: as fp8z1_step_fused; EINVAL when either set is out of domain. */
+int fp8z1_step_fused_select(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp_if_clear,
+                            const fp8z1_adamw_hp* hp_if_set, const int32_t* d_select, const float* grad_shard,
+                            const float* const* d_grad_params, float* master_shard, float* m_shard,
+                            float* v_shard, uint8_t* fp8_shard, uint8_t* const* d_fp8_params, float* scale_shard,
+                            int64_t b0, int64_t b1, const double* d_sumsq, const int32_t* d_found_inf,
+                            void* stream);
+
 /* ---- the step with its scalars in device memory (for CUDA graphs) --------- */
 
 /* The FP32 scalars one step uses, derived on the host in double from

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
 from blockwise_fp8_zero_fold_gb300 import synth
 from blockwise_fp8_zero_fold_gb300.optimizer import ShardOptimizer
 from tests._gpu import lib  # noqa: F401
@@ -165,3 +166,44 @@ def test_unit_scale_blocks_counts_zero_blocks(lib):
     g[0][3].zero_()
     assert opt.step(g) == 0
     assert opt.stats()["unit_scale_blocks"] == 2
+
+
+def test_async_steps_equal_synchronous_steps(lib):
+    """Eight steps enqueued ahead of their found_inf (launch_step_async: each
+    step's t and S picked on the device by the previous step's flag), with
+    skips at steps 3, 4 and 7 and the scale growing every 2 clean steps: the
+    state, FP8 weights, scales and loss scaler equal the synchronous path's."""
+    w = synth.workload("tiny", shapes=[(3, 512, 384), (1, 1000, 131), (2, 130, 260)], dp=1, rank=0,
+                       m_sigma=1e-4, v_sigma=1e-8, max_norm=0.5)
+    sync, asy = _make(w, 0), _make(w, 0)
+    for o in (sync, asy):
+        o.init_state(*(synth.make_state(w, k, "cuda") for k in ("master", "m", "v")))
+    f_sync = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w.shapes]
+    f_asy = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w.shapes]
+    bad = {3, 4, 7}
+    gs = []
+    for t in range(1, 9):
+        g = synth.make_grads(w, t, "cuda")
+        if t in bad:
+            g[t % 3][0, 3, 5] = float("nan")
+        gs.append(g)
+    want = [sync.step(g, f_sync) for g in gs]
+    got = []
+    g_dev = [torch.empty_like(x) for x in gs[0]]
+    for g in gs:
+        for d, x in zip(g_dev, g):
+            d.copy_(x)  # the same grad tensors every step, refilled in stream order
+        got += asy.launch_step_async(g_dev, f_asy)
+    got += asy.drain()
+    assert want == got == [int(t in bad) for t in range(1, 9)]
+    assert (asy.scaler.scale, asy.scaler.step, asy.scaler.good_steps) == \
+        (sync.scaler.scale, sync.scaler.step, sync.scaler.good_steps)
+    for name in ("master", "m", "v", "scales"):
+        assert torch.equal(getattr(sync, name).view(torch.int32), getattr(asy, name).view(torch.int32)), name
+    for a, b in zip(f_sync, f_asy):
+        assert torch.equal(a, b)
+    assert asy.stats()["step"] == 5 and F.fp8z1_device_status(asy.layout) == 0
+    with pytest.raises(RuntimeError):  # no synchronous step while async steps are in flight
+        asy.launch_step_async(g_dev, f_asy)
+        asy.step(g_dev, f_asy)
+    asy.drain()
