@@ -1,6 +1,8 @@
-"""GPU parity on the workloads at their full sizes, through the C-ABI in the
-configuration bench.py times (fold all grads -> per-rank norm partials summed
--> fused step on the rank's range -> unfold the codes).
+"""GPU parity on the workloads at their full sizes, through the C-ABI: the
+unfused entry points (fold all grads -> per-rank norm partials summed ->
+step on the rank's range -> unfold the codes) on every workload, and the MoE
+buffer in the loop bench.py times (fused, steps enqueued ahead of their
+found_inf), with a check of every block against the quantiser's definition.
 
 The oracle checks every step on a seeded sample of blocks, one block at a
 time: blocks are independent given the global scalars ("面向 Blockwise FP8
@@ -223,3 +225,78 @@ def test_large_two_steps_and_bf16_fold(lib):
     torch.cuda.synchronize()
     for a, b in zip(bf, back):  # unfold(fold(x)) == x over every element
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_moe_in_the_bench_loop_every_block(lib):
+    """The MoE buffer in exactly the loop bench.py times: ShardOptimizer on the
+    fused path, steps enqueued ahead of their found_inf (launch_step_async),
+    the same grads every step.  After three steps: sampled blocks against the
+    oracle (master / m / v / scales bit-exact, the row-major FP8 tiles), the
+    norm against the exact sum, and on every block of the buffer the
+    quantiser's definition ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结):
+    scale = amax/448 (1 when amax = 0) of the new FP32 master, codes = the
+    E4M3 round-to-nearest-even of master/scale (torch.float8_e4m3fn casts)."""
+    from blockwise_fp8_zero_fold_gb300.optimizer import ShardOptimizer
+    w = synth.workload("moe", dp=1, rank=0)
+    dev = torch.device("cuda")
+    opt = ShardOptimizer(w.shapes, loss_scale=w.loss_scale, growth_interval=w.growth_interval,
+                         **{k: v for k, v in w.hp().items() if k != "loss_scale"})
+    lut = oracle.build_lut(w.shapes)
+    rng = np.random.default_rng(77)
+    tiles = synth.zero_tiles(w)
+    cb0 = -(-w.shapes[0][2] // 128)
+    rb0 = -(-w.shapes[0][1] // 128)
+    sample = sorted(set(int(x) for x in rng.choice(opt.nblk, 120, replace=False))
+                    | {0, opt.nblk - 1} | {int((e * rb0 + a) * cb0 + b) for e, a, b in tiles[0][:3].tolist()})
+
+    def tile(rm, k):
+        p, e, rb, cb, rr, cr = (int(x) for x in lut[k])
+        return rm[p][e, 128 * rb:128 * rb + rr, 128 * cb:128 * cb + cr]
+
+    def oblock(rm, k):
+        t = np.ascontiguousarray(to_host(tile(rm, k)))
+        return oracle.fold([(1,) + t.shape], [t.reshape((1,) + t.shape)])
+
+    state = {}
+    for kind in ("master", "m", "v"):
+        rm = synth.make_state(w, kind, dev)
+        opt.fold_into(rm, getattr(opt, kind))
+        state[kind] = [oblock(rm, k) for k in sample]
+        del rm
+    grads = synth.make_grads(w, 1, dev)
+    fp8 = [torch.full(s, 0x7F, dtype=torch.uint8, device=dev) for s in w.shapes]
+    found = []
+    for _ in range(3):
+        found += opt.launch_step_async(grads, fp8)
+    found += opt.drain()
+    assert found == [0, 0, 0] and opt.scaler.step == 3
+
+    exact, fi = oracle.sumsq_parallel([to_host(g) for g in grads], threads=16)
+    assert fi == 0 and abs(float(opt.sumsq.item()) - exact) <= 1e-12 * exact
+    for i, k in enumerate(sample):
+        g = oblock(grads, k)
+        for t in range(1, 4):
+            q, sc, _ = oracle.step(oracle.make_hp(step=t, **w.hp()), exact, 0, g, state["master"][i],
+                                   state["m"][i], state["v"][i])
+        for name in ("master", "m", "v"):
+            got = to_host(getattr(opt, name)[k * B:(k + 1) * B])
+            assert np.array_equal(got.view(np.uint32), state[name][i].view(np.uint32)), (name, k)
+        assert float(opt.scales[k]) == float(sc[0])
+        p, e, rb, cb, rr, cr = (int(x) for x in lut[k])
+        want = np.zeros((1, rr, cr), np.uint8)
+        oracle.unfold([(1, rr, cr)], q, [want])
+        assert np.array_equal(to_host(tile(fp8, k)), want[0]), k
+
+    # every block: the scale and the codes from their definitions
+    master = opt.master.view(opt.nblk, B)
+    amax = master.abs().amax(dim=1)
+    # a tensor divisor: torch divides by a Python scalar through its reciprocal,
+    # which can be an ulp off the IEEE quotient the definition asks for
+    want_scale = torch.where(amax == 0, torch.ones_like(amax), amax / torch.full_like(amax, 448.0))
+    assert torch.equal(opt.scales.view(torch.int32), want_scale.view(torch.int32))
+    folded = torch.empty(opt.nblk * B, dtype=torch.uint8, device=dev)
+    F.fp8z1_fold(opt.layout, F.param_pointers(fp8), folded, 1, 0, opt.nblk)
+    want_codes = (master / want_scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).view(-1)
+    assert torch.equal(folded, want_codes)
+    assert (opt.scales == 1.0).sum().item() >= len(tiles[0]) + len(tiles[1])  # the all-zero tiles
+    assert F.fp8z1_device_status(opt.layout) == 0
