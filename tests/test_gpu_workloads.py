@@ -227,8 +227,11 @@ def test_large_two_steps_and_bf16_fold(lib):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_moe_in_the_bench_loop_every_block(lib):
-    """The MoE buffer in exactly the loop bench.py times: ShardOptimizer on the
+@pytest.mark.parametrize("name", ["moe", "ragged", "dense"])
+def test_bench_loop_every_block(lib, name):
+    """A workload's whole buffer in exactly the loop bench.py times (MoE: the
+    bench's default; ragged: the padding-aware step kernel on partial blocks;
+    dense: both kernels, full-tile runs and a padded param): ShardOptimizer on the
     fused path, steps enqueued ahead of their found_inf (launch_step_async),
     the same grads every step.  After three steps: sampled blocks against the
     oracle (master / m / v / scales bit-exact, the row-major FP8 tiles), the
@@ -237,7 +240,7 @@ def test_moe_in_the_bench_loop_every_block(lib):
     scale = amax/448 (1 when amax = 0) of the new FP32 master, codes = the
     E4M3 round-to-nearest-even of master/scale (torch.float8_e4m3fn casts)."""
     from blockwise_fp8_zero_fold_gb300.optimizer import ShardOptimizer
-    w = synth.workload("moe", dp=1, rank=0)
+    w = synth.workload(name, dp=1, rank=0)
     dev = torch.device("cuda")
     opt = ShardOptimizer(w.shapes, loss_scale=w.loss_scale, growth_interval=w.growth_interval,
                          **{k: v for k, v in w.hp().items() if k != "loss_scale"})
