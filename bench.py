@@ -441,7 +441,11 @@ def bench_mx(args, rank, world, dist):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        opt.step(grad)
+        if args.pipeline:
+            opt.launch_step_async(grad)
+        else:
+            opt.step(grad)
+    opt.drain()
     torch.cuda.synchronize()
     ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)] for k in ("norm", "step")}
@@ -457,7 +461,10 @@ def bench_mx(args, rank, world, dist):
     n0 = F.fp8z1_kernel_launches()
     t0.record(stream)
     skipped = 0
-    for i in range(args.steps):
+    for i in range(args.steps if args.pipeline else 0):  # steps ahead of their found_inf
+        skipped += sum(opt.launch_step_async(grad, stream, {"norm": ev["norm"][i], "step": ev["step"][i]}))
+    skipped += sum(opt.drain())
+    for i in range(0 if args.pipeline else args.steps):
         ev["norm"][i][0].record(stream)
         F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
         F.fp8z1_mx_grad_norm(opt.layout, grad, opt.g0, opt.g1, opt.sumsq, opt.found_inf)
@@ -491,7 +498,8 @@ def bench_mx(args, rank, world, dist):
         "scheme": "mx", "gpu_launches": launches, "kernels_ms": kern,
         "kernels_gbs": {"norm": 4 * n / kern["norm"] / 1e6, "step": achieved},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "fp8z1_mx_step",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "fp8z1_mx_step_select" if args.pipeline else "fp8z1_mx_step",
                      "peak_source": peak_kind, "bytes_per_launch": step_bytes},
         "clocks": clk, "skipped_steps": skipped, "e2e": None,
     }
@@ -658,9 +666,10 @@ def main():
     ap.add_argument("--compare", type=int, default=1, help="also time the other path briefly")
     ap.add_argument("--experts", type=int, default=0,
                     help="keep only the first K experts of each 3-D param (a smaller case)")
-    ap.add_argument("--pipeline", type=int, default=1,
-                    help="fused path: enqueue each step before the previous one's found_inf is read "
-                         "(ShardOptimizer.launch_step_async)")
+    ap.add_argument("--pipeline", type=int, default=-1,
+                    help="enqueue each step before the previous one's found_inf is read "
+                         "(launch_step_async); -1: on for the block scheme's fused path, off for MX, "
+                         "whose select kernel runs 2-3%% slower than its plain one")
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)
@@ -671,6 +680,8 @@ def main():
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=1)
     args = ap.parse_args()
+    if args.pipeline < 0:
+        args.pipeline = int(args.scheme == "block" and args.path == "fused")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 

@@ -11,6 +11,11 @@
 // and saturated at 448.  The update is update.cuh's, bit for bit the
 // block-wise one.  There is no table and no CTA barrier: a group is 8
 // consecutive lanes (one float4 each), its amax three shuffles.
+//
+// fp8z1_mx_step_select runs the same body with a second scalar set picked by
+// a device flag, in its own kernel with its own argument struct: adding
+// fields to MxArgs alone changed the plain kernel's register allocation (65 to
+// 59 registers) and cost it about 4% (6.12 to 6.36 ms on the MoE buffer).
 #include "update.cuh"
 
 namespace {
@@ -31,19 +36,24 @@ struct MxArgs {
     StepScalars c;
 };
 
+// The select kernel's arguments: the plain step's, the second scalar set and
+// the flag that picks it (kept apart from MxArgs, whose layout the plain
+// kernel's code generation is tuned on).
+struct MxSelArgs {
+    MxArgs a;
+    const int32_t* select;  // a.c when *select == 0, else c2
+    StepScalars c2;
+};
+
 // Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
 // u, its 32 lanes hold 4 whole groups) and issues every load of them before
 // any update; with 3 CTAs resident per SM (24 warps) that keeps about 96 KB
 // of loads in flight per SM.
 constexpr int kMxUnroll = 2;
 
-__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
+// The update and quantise of this warp's chunks, with the scalars c.
+__device__ __forceinline__ void mx_body(const MxArgs& a, const StepScalars& c, float gs)
 {
-    if (*a.found_inf != 0) return;  // skipped step: write nothing
-    __shared__ float s_gscale;
-    if (threadIdx.x == 0) s_gscale = grad_factor(*a.sumsq, a.c);
-    __syncthreads();
-    const float gs = s_gscale;
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kMxThreads / 32);
@@ -68,10 +78,10 @@ __global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
             const int64_t i = wbase + u * 32 + lane;
             const bool valid = i < a.n_chunks;
             if (valid) {
-                adamw(gs, a.c, g4[u].x, p4[u].x, m4[u].x, v4[u].x);
-                adamw(gs, a.c, g4[u].y, p4[u].y, m4[u].y, v4[u].y);
-                adamw(gs, a.c, g4[u].z, p4[u].z, m4[u].z, v4[u].z);
-                adamw(gs, a.c, g4[u].w, p4[u].w, m4[u].w, v4[u].w);
+                adamw(gs, c, g4[u].x, p4[u].x, m4[u].x, v4[u].x);
+                adamw(gs, c, g4[u].y, p4[u].y, m4[u].y, v4[u].y);
+                adamw(gs, c, g4[u].z, p4[u].z, m4[u].z, v4[u].z);
+                adamw(gs, c, g4[u].w, p4[u].w, m4[u].w, v4[u].w);
                 __stcs(a.mom1 + i, m4[u]);
                 __stcs(a.mom2 + i, v4[u]);
                 __stcs(a.master + i, p4[u]);
@@ -99,22 +109,48 @@ __global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
     }
 }
 
-}  // namespace
-
-extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
-                             float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
-                             uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
-                             const int32_t* d_found_inf, void* stream)
+// Scalars by value (the plain step).
+__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
 {
-    fp8z1::NvtxRange nvtx_range("fp8z1_mx_step");
+    if (*a.found_inf != 0) return;  // skipped step: write nothing
+    __shared__ float s_gscale;
+    if (threadIdx.x == 0) s_gscale = grad_factor(*a.sumsq, a.c);
+    __syncthreads();
+    mx_body(a, a.c, s_gscale);
+}
+
+// Two scalar sets by value, picked by *select behind one uniform branch.
+__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel_select(const MxSelArgs sa)
+{
+    if (*sa.a.found_inf != 0) return;  // skipped step: write nothing
+    __shared__ float s_gscale;
+    __shared__ int s_alt;
+    if (threadIdx.x == 0) {
+        const bool alt = *sa.select != 0;
+        s_alt = alt;
+        s_gscale = grad_factor(*sa.a.sumsq, alt ? sa.c2 : sa.a.c);
+    }
+    __syncthreads();
+    if (s_alt)
+        mx_body(sa.a, sa.c2, s_gscale);
+    else
+        mx_body(sa.a, sa.a.c, s_gscale);
+}
+
+int mx_step_impl(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const fp8z1_adamw_hp* hp_if_set,
+                 const int32_t* d_select, const float* grad_shard, float* master_shard, float* m_shard,
+                 float* v_shard, uint8_t* fp8_shard, uint8_t* scale_shard, int64_t g0, int64_t g1,
+                 const double* d_sumsq, const int32_t* d_found_inf, void* stream)
+{
     if (!L || !hp || !grad_shard || !master_shard || !m_shard || !v_shard || !fp8_shard || !scale_shard ||
-        !d_sumsq || !d_found_inf || !in_domain(hp))
+        !d_sumsq || !d_found_inf || !in_domain(hp) || (hp_if_set && !in_domain(hp_if_set)))
         return FP8Z1_EINVAL;
+    if ((hp_if_set == nullptr) != (d_select == nullptr)) return FP8Z1_EINVAL;
     if (g0 < 0 || g1 < g0 || g1 > L->n_groups) return FP8Z1_EINVAL;
     if (!L->on_device) return FP8Z1_ENODEV;
     if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(master_shard, 16) || !fp8z1::aligned(m_shard, 16) ||
         !fp8z1::aligned(v_shard, 16) || !fp8z1::aligned(fp8_shard, 16) || !fp8z1::aligned(d_sumsq, 8) ||
-        !fp8z1::aligned(d_found_inf, 4))
+        !fp8z1::aligned(d_found_inf, 4) || (d_select && !fp8z1::aligned(d_select, 4)))
         return FP8Z1_EALIGN;
     const int64_t chunks = (g1 - g0) * (FP8Z1_MX_GROUP / 4);
     if (chunks == 0) return FP8Z1_OK;
@@ -134,6 +170,39 @@ extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp,
     const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
     if (grid > need) grid = need;
     fp8z1::count_launch();
-    mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d_select) {
+        MxSelArgs sa = {};
+        sa.a = a;
+        sa.select = d_select;
+        sa.c2 = scalars(hp_if_set);
+        mx_step_kernel_select<<<(unsigned)grid, kMxThreads, 0, s>>>(sa);
+    } else {
+        mx_step_kernel<<<(unsigned)grid, kMxThreads, 0, s>>>(a);
+    }
     return fp8z1::launch_status();
+}
+
+}  // namespace
+
+extern "C" int fp8z1_mx_step_select(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp_if_clear,
+                                    const fp8z1_adamw_hp* hp_if_set, const int32_t* d_select,
+                                    const float* grad_shard, float* master_shard, float* m_shard, float* v_shard,
+                                    uint8_t* fp8_shard, uint8_t* scale_shard, int64_t g0, int64_t g1,
+                                    const double* d_sumsq, const int32_t* d_found_inf, void* stream)
+{
+    fp8z1::NvtxRange nvtx_range("fp8z1_mx_step_select");
+    if (!hp_if_set || !d_select) return FP8Z1_EINVAL;
+    return mx_step_impl(L, hp_if_clear, hp_if_set, d_select, grad_shard, master_shard, m_shard, v_shard, fp8_shard,
+                        scale_shard, g0, g1, d_sumsq, d_found_inf, stream);
+}
+
+extern "C" int fp8z1_mx_step(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const float* grad_shard,
+                             float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                             uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
+                             const int32_t* d_found_inf, void* stream)
+{
+    fp8z1::NvtxRange nvtx_range("fp8z1_mx_step");
+    return mx_step_impl(L, hp, nullptr, nullptr, grad_shard, master_shard, m_shard, v_shard, fp8_shard, scale_shard,
+                        g0, g1, d_sumsq, d_found_inf, stream);
 }

@@ -101,6 +101,8 @@ _SIGS = {
     "fp8z1_mx_grad_norm": (C.c_int, [_P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_mx_step": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), _P, _P, _P, _P, _P, _P, C.c_int64,
                                 C.c_int64, _P, _P, _P]),
+    "fp8z1_mx_step_select": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_adamw_hp), _P, _P, _P,
+                                       _P, _P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_scaler_update": (C.c_int, [C.POINTER(fp8z1_loss_scaler), C.c_int32]),
     "fp8z1_clip_coef": (C.c_int, [C.c_double, C.c_float, C.c_float, C.POINTER(C.c_double),
                                   C.POINTER(C.c_double)]),
@@ -405,6 +407,16 @@ def fp8z1_mx_step(layout: MxLayout, hp: fp8z1_adamw_hp, grad_shard, master_shard
                                _ptr(m_shard), _ptr(v_shard), _ptr(fp8_shard), _ptr(scale_shard),
                                int(g0), int(g1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_mx_step")
+
+
+def fp8z1_mx_step_select(layout: MxLayout, hp_if_clear: fp8z1_adamw_hp, hp_if_set: fp8z1_adamw_hp, d_select,
+                         grad_shard, master_shard, m_shard, v_shard, fp8_shard, scale_shard, g0: int, g1: int,
+                         d_sumsq, d_found_inf, stream=None):
+    """fp8z1_mx_step with ``hp_if_clear`` when *d_select == 0, else ``hp_if_set``."""
+    _check(lib().fp8z1_mx_step_select(layout.handle, C.byref(hp_if_clear), C.byref(hp_if_set), _ptr(d_select),
+                                      _ptr(grad_shard), _ptr(master_shard), _ptr(m_shard), _ptr(v_shard),
+                                      _ptr(fp8_shard), _ptr(scale_shard), int(g0), int(g1), _ptr(d_sumsq),
+                                      _ptr(d_found_inf), _stream(stream)), "fp8z1_mx_step_select")
 
 
 def fp8z1_clip_coef(sumsq: float, max_norm: float, loss_scale: float):

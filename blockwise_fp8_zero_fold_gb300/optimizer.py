@@ -29,7 +29,97 @@ import torch
 from . import fp8z1 as F
 
 
-class ShardOptimizer:
+class _AsyncSteps:
+    """Steps enqueued ahead of their found_inf, shared by both optimizers.
+
+    The method reads found_inf after every step to set the next step's t
+    and S ("DeepSpeed ZeRO 优化" §六).  Here the host reads it one step late:
+    while step k-1 may still run, step k is enqueued with both candidate
+    hyper-parameter sets (step k-1 clean: t+1 and S after growth; skipped: t
+    and S/2), and its kernel picks one by step k-1's found_inf (the *_select
+    entry points).  Each step's norm accumulators alternate between two slots,
+    and its found_inf is copied to pinned memory right after its norm; the
+    host waits only for that copy of step k-2 before enqueuing step k.
+    Results equal the synchronous steps'."""
+
+    def _async_launch(self, norm, step, stream, events) -> List[int]:
+        """norm(sumsq, found, s) enqueues the norm; step(hp, hp_if_set,
+        d_select, sumsq, found, s) the update (hp_if_set / d_select None when
+        no step is unresolved)."""
+        st = getattr(self, "_async", None)
+        if st is None:
+            st = self._async = {
+                "sumsq": torch.zeros(2, dtype=torch.float64, device=self.device),
+                "found": torch.zeros(2, dtype=torch.int32, device=self.device),
+                "flags": [torch.zeros(1, dtype=torch.int32, pin_memory=True) for _ in range(2)],
+                "done": [torch.cuda.Event() for _ in range(2)],
+                "k": 0, "inflight": [],  # slots of unresolved steps, oldest first
+            }
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        resolved = []
+        while len(st["inflight"]) >= 2:  # resolve step k-2: its flag copy ran long ago
+            resolved.append(self._resolve_async())
+        slot = st["k"] % 2
+        st["k"] += 1
+        sumsq, found = st["sumsq"][slot:slot + 1], st["found"][slot:slot + 1]
+        ev = events or {}
+        if "norm" in ev:
+            ev["norm"][0].record(s)
+        F.fp8z1_norm_reset(sumsq, found, s)
+        norm(sumsq, found, s)
+        if self.norm_hook is not None:
+            with torch.cuda.stream(s):
+                self.norm_hook(sumsq, found)
+        if "norm" in ev:
+            ev["norm"][1].record(s)
+        with torch.cuda.stream(s):
+            st["flags"][slot].copy_(found, non_blocking=True)
+        st["done"][slot].record(s)
+        if "step" in ev:
+            ev["step"][0].record(s)
+        if not st["inflight"]:
+            step(self._hp_after(None), None, None, sumsq, found, s)
+        else:
+            prev = st["inflight"][0]
+            step(self._hp_after(0), self._hp_after(1), st["found"][prev:prev + 1], sumsq, found, s)
+        if "step" in ev:
+            ev["step"][1].record(s)
+        st["inflight"].append(slot)
+        # the latest step's accumulators, for stats() once drained
+        self.sumsq, self.found_inf = sumsq, found
+        return resolved
+
+    def _async_busy(self) -> bool:
+        st = getattr(self, "_async", None)
+        return st is not None and bool(st["inflight"])
+
+    def _hp_after(self, found_prev: Optional[int]):
+        """The hyper-parameters of the next step, given the resolved scaler and,
+        when one step is unresolved, its found_inf."""
+        sc = self.scaler
+        if found_prev is not None:
+            sc = F.fp8z1_loss_scaler(sc.scale, sc.step, sc.good_steps, sc.growth_interval)
+            F.fp8z1_scaler_update(sc, int(found_prev))
+        return F.make_hp(step=sc.step + 1, loss_scale=sc.scale, **self.hp)
+
+    def _resolve_async(self) -> int:
+        st = self._async
+        slot = st["inflight"].pop(0)
+        st["done"][slot].synchronize()
+        found = int(st["flags"][slot].item())
+        F.fp8z1_scaler_update(self.scaler, found)
+        return found
+
+    def drain(self) -> List[int]:
+        """Wait for every step enqueued by ``launch_step_async`` and return
+        their found_inf, oldest first (the loss scaler and t then count them)."""
+        out = []
+        while self._async_busy():
+            out.append(self._resolve_async())
+        return out
+
+
+class ShardOptimizer(_AsyncSteps):
     def __init__(self, shapes: Sequence[Sequence[int]], *, dp_size: int = 1, rank: int = 0,
                  lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=1.0,
                  loss_scale=1024.0, growth_interval=1000, device="cuda", fused: bool = True):
@@ -117,6 +207,7 @@ class ShardOptimizer:
         v, the codes and scales, and the host scalars (t, S, clean-step count).
         The buffers are the 1-D block layout itself, so a reload is a copy."""
         self.finish_host_step()
+        self.drain()
         return {
             "shapes": [tuple(s) for s in self.shapes], "b0": self.b0, "b1": self.b1,
             "master": self.master.cpu(), "m": self.m.cpu(), "v": self.v.cpu(),
@@ -128,6 +219,7 @@ class ShardOptimizer:
 
     def load_state_dict(self, sd: dict):
         self.finish_host_step()
+        self.drain()
         if [tuple(s) for s in sd["shapes"]] != [tuple(s) for s in self.shapes] or \
                 (sd["b0"], sd["b1"]) != (self.b0, self.b1):
             raise ValueError("checkpoint was taken for another layout or shard")
@@ -144,7 +236,7 @@ class ShardOptimizer:
         """Enqueue one step (no host synchronisation)."""
         if self._host_pending is not None:
             raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
-        if self._async is not None and self._async["inflight"]:
+        if self._async_busy():
             raise RuntimeError("steps from launch_step_async are in flight: call drain() first")
         F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
@@ -215,7 +307,7 @@ class ShardOptimizer:
         ``finish_host_step``, which also waits for the copies back: the host
         FP8 weights and scales are complete only after it."""
         assert self.fused, "step_from_host runs the fused path"
-        if self._async is not None and self._async["inflight"]:
+        if self._async_busy():
             raise RuntimeError("steps from launch_step_async are in flight: call drain() first")
         if (self.b0, self.b1) != (0, self.nblk):
             raise ValueError("step_from_host needs the whole buffer as the shard (dp_size 1)")
@@ -304,99 +396,32 @@ class ShardOptimizer:
     # -- steps enqueued ahead of their found_inf --------------------------------
     def launch_step_async(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
                           stream=None, events: Optional[dict] = None) -> List[int]:
-        """Enqueue one fused step without waiting for the previous one.
-
-        The method reads found_inf after every step to set the next step's t
-        and S ("DeepSpeed ZeRO 优化" §六).  Here the host reads it one step
-        late: while step k-1 may still run, step k is enqueued with both
-        candidate hyper-parameter sets (step k-1 clean: t+1 and S after growth;
-        skipped: t and S/2), and the kernel picks one by step k-1's found_inf
-        (fp8z1_step_fused_select).  Each step's norm accumulators alternate
-        between two slots, and its found_inf is copied to pinned memory right
-        after its norm; the host waits only for that copy of step k-2 before
-        enqueuing step k.  Results equal ``step`` run one at a time.
-
-        Returns the found_inf of the steps resolved by this call (oldest
-        first); ``drain`` resolves the rest.  ``events``: optional
-        {"norm": (start, end), "step": (start, end)} CUDA events to record
-        around the two kernels on ``stream``."""
+        """Enqueue one fused step without waiting for the previous one
+        (``_AsyncSteps``; fp8z1_step_fused_select).  Returns the found_inf of
+        the steps resolved by this call, oldest first; ``drain`` resolves the
+        rest.  ``events``: optional {"norm": (start, end), "step": (start,
+        end)} CUDA events to record around the two kernels on ``stream``."""
         if not self.fused:
             raise ValueError("launch_step_async runs the fused path")
         if self._host_pending is not None:
             raise RuntimeError("a step_from_host(wait=False) is in flight: call finish_host_step() first")
-        st = self._async
-        if st is None:
-            st = self._async = {
-                "sumsq": torch.zeros(2, dtype=torch.float64, device=self.device),
-                "found": torch.zeros(2, dtype=torch.int32, device=self.device),
-                "flags": [torch.zeros(1, dtype=torch.int32, pin_memory=True) for _ in range(2)],
-                "done": [torch.cuda.Event() for _ in range(2)],
-                "k": 0, "inflight": [],  # slots of unresolved steps, oldest first
-            }
-        s = stream if stream is not None else torch.cuda.current_stream(self.device)
-        resolved = []
-        while len(st["inflight"]) >= 2:  # resolve step k-2: its flag copy ran long ago
-            resolved.append(self._resolve_async())
-        slot = st["k"] % 2
-        st["k"] += 1
-        sumsq, found = st["sumsq"][slot:slot + 1], st["found"][slot:slot + 1]
         gptrs = self._ptrs(grads)
-        ev = events or {}
-        if "norm" in ev:
-            ev["norm"][0].record(s)
-        F.fp8z1_norm_reset(sumsq, found, s)
-        F.fp8z1_fold_norm(self.layout, gptrs, None, self.b0, self.b1, sumsq, found, s)
-        if self.norm_hook is not None:
-            with torch.cuda.stream(s):
-                self.norm_hook(sumsq, found)
-        if "norm" in ev:
-            ev["norm"][1].record(s)
-        with torch.cuda.stream(s):
-            st["flags"][slot].copy_(found, non_blocking=True)
-        st["done"][slot].record(s)
-        kw = dict(d_grad_params=gptrs, master_shard=self.master, m_shard=self.m, v_shard=self.v,
-                  fp8_shard=self.codes if fp8_params is None else None,
-                  d_fp8_params=None if fp8_params is None else self._ptrs(fp8_params),
-                  scale_shard=self.scales, b0=self.b0, b1=self.b1, d_sumsq=sumsq, d_found_inf=found, stream=s)
-        if "step" in ev:
-            ev["step"][0].record(s)
-        if not st["inflight"]:
-            F.fp8z1_step_fused(self.layout, self._hp_after(None), **kw)
-        else:
-            prev = st["inflight"][0]
-            F.fp8z1_step_fused_select(self.layout, self._hp_after(0), self._hp_after(1),
-                                      st["found"][prev:prev + 1], **kw)
-        if "step" in ev:
-            ev["step"][1].record(s)
-        st["inflight"].append(slot)
-        # the latest step's accumulators, for stats() once drained
-        self.sumsq, self.found_inf = sumsq, found
-        return resolved
+        fptrs = None if fp8_params is None else self._ptrs(fp8_params)
 
-    def _hp_after(self, found_prev: Optional[int]):
-        """The hyper-parameters of the next step, given the resolved scaler and,
-        when one step is unresolved, its found_inf."""
-        sc = self.scaler
-        if found_prev is not None:
-            sc = F.fp8z1_loss_scaler(sc.scale, sc.step, sc.good_steps, sc.growth_interval)
-            F.fp8z1_scaler_update(sc, int(found_prev))
-        return F.make_hp(step=sc.step + 1, loss_scale=sc.scale, **self.hp)
+        def norm(sumsq, found, s):
+            F.fp8z1_fold_norm(self.layout, gptrs, None, self.b0, self.b1, sumsq, found, s)
 
-    def _resolve_async(self) -> int:
-        st = self._async
-        slot = st["inflight"].pop(0)
-        st["done"][slot].synchronize()
-        found = int(st["flags"][slot].item())
-        F.fp8z1_scaler_update(self.scaler, found)
-        return found
+        def step(hp, hp_set, select, sumsq, found, s):
+            kw = dict(d_grad_params=gptrs, master_shard=self.master, m_shard=self.m, v_shard=self.v,
+                      fp8_shard=self.codes if fptrs is None else None, d_fp8_params=fptrs,
+                      scale_shard=self.scales, b0=self.b0, b1=self.b1, d_sumsq=sumsq, d_found_inf=found,
+                      stream=s)
+            if hp_set is None:
+                F.fp8z1_step_fused(self.layout, hp, **kw)
+            else:
+                F.fp8z1_step_fused_select(self.layout, hp, hp_set, select, **kw)
 
-    def drain(self) -> List[int]:
-        """Wait for every step enqueued by ``launch_step_async`` and return
-        their found_inf, oldest first (the loss scaler and t then count them)."""
-        out = []
-        while self._async is not None and self._async["inflight"]:
-            out.append(self._resolve_async())
-        return out
+        return self._async_launch(norm, step, stream, events)
 
     def finish_step(self) -> int:
         """Read found_inf (synchronises) and update the loss scale and t."""
@@ -422,6 +447,7 @@ class ShardOptimizer:
         many of this shard's blocks have scale 1 (amax 0 -- an all-zero block
         -- or exactly 448)."""
         self.finish_host_step()
+        self.drain()
         s = float(self.sumsq.item())
         found = int(self.found_inf.item())
         used = self.scaler.scale if loss_scale is None else loss_scale
@@ -528,7 +554,7 @@ class CapturedStep:
         return self.opt.finish_step()
 
 
-class MxShardOptimizer:
+class MxShardOptimizer(_AsyncSteps):
     """The same optimizer step with MXFP8 weights (E8M0 scale per 32
     consecutive elements) instead of 128x128 blocks.
 
@@ -565,7 +591,26 @@ class MxShardOptimizer:
         """This rank's slice of a whole flat buffer (grads, say)."""
         return flat[self.g0 * F.MX_GROUP:self.g1 * F.MX_GROUP]
 
+    def launch_step_async(self, grad_shard: torch.Tensor, stream=None, events: Optional[dict] = None) -> List[int]:
+        """Enqueue one step without waiting for the previous one (``_AsyncSteps``;
+        fp8z1_mx_step_select).  Returns the found_inf of the steps resolved by
+        this call; ``drain`` resolves the rest."""
+        def norm(sumsq, found, s):
+            F.fp8z1_mx_grad_norm(self.layout, grad_shard, self.g0, self.g1, sumsq, found, s)
+
+        def step(hp, hp_set, select, sumsq, found, s):
+            args = (grad_shard, self.master, self.m, self.v, self.codes, self.scales, self.g0, self.g1, sumsq,
+                    found, s)
+            if hp_set is None:
+                F.fp8z1_mx_step(self.layout, hp, *args)
+            else:
+                F.fp8z1_mx_step_select(self.layout, hp, hp_set, select, *args)
+
+        return self._async_launch(norm, step, stream, events)
+
     def launch_step(self, grad_shard: torch.Tensor, stream=None):
+        if self._async_busy():
+            raise RuntimeError("steps from launch_step_async are in flight: call drain() first")
         F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         F.fp8z1_mx_grad_norm(self.layout, grad_shard, self.g0, self.g1, self.sumsq, self.found_inf,
                              stream)
@@ -586,6 +631,7 @@ class MxShardOptimizer:
 
     # -- checkpoint / resume and logging, as ShardOptimizer's ------------------
     def state_dict(self) -> dict:
+        self.drain()
         return {
             "shapes": [tuple(s) for s in self.shapes], "g0": self.g0, "g1": self.g1,
             "master": self.master.cpu(), "m": self.m.cpu(), "v": self.v.cpu(),
@@ -596,6 +642,7 @@ class MxShardOptimizer:
         }
 
     def load_state_dict(self, sd: dict):
+        self.drain()
         if [tuple(s) for s in sd["shapes"]] != [tuple(s) for s in self.shapes] or \
                 (sd["g0"], sd["g1"]) != (self.g0, self.g1):
             raise ValueError("checkpoint was taken for another layout or shard")
@@ -609,6 +656,7 @@ class MxShardOptimizer:
     def stats(self, loss_scale: Optional[float] = None) -> dict:
         """The last step's global norm, clip coefficient, skip, t and S, and how
         many of this shard's groups have scale 1 (E8M0 code 127)."""
+        self.drain()
         s = float(self.sumsq.item())
         found = int(self.found_inf.item())
         used = self.scaler.scale if loss_scale is None else loss_scale

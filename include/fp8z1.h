@@ -397,6 +397,16 @@ int fp8z1_mx_step(const fp8z1_mx_layout* layout, const fp8z1_adamw_hp* hp, const
                   uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
                   const int32_t* d_found_inf, void* stream);
 
+/* fp8z1_mx_step with two candidate hyper-parameter sets, as
+ * fp8z1_step_fused_select: `hp_if_clear` when *d_select == 0 (device, 4-byte
+ * aligned, read when the kernel runs), `hp_if_set` otherwise.
+ * Errors: as fp8z1_mx_step. */
+int fp8z1_mx_step_select(const fp8z1_mx_layout* layout, const fp8z1_adamw_hp* hp_if_clear,
+                         const fp8z1_adamw_hp* hp_if_set, const int32_t* d_select, const float* grad_shard,
+                         float* master_shard, float* m_shard, float* v_shard, uint8_t* fp8_shard,
+                         uint8_t* scale_shard, int64_t g0, int64_t g1, const double* d_sumsq,
+                         const int32_t* d_found_inf, void* stream);
+
 /* ---- loss scaling (host; "DeepSpeed ZeRO 优化" §六, §九 Q6) ---------------- */
 
 /* After a step whose found_inf flag the host has read: found_inf != 0 halves

@@ -268,3 +268,31 @@ def test_mx_optimizer_resume_is_bit_identical(lib):
     assert st["unit_scale_groups"] == int((second.scales == 127).sum())
     with pytest.raises(ValueError):
         MxShardOptimizer(shapes, dp_size=2, rank=0, **hp).load_state_dict(ref.state_dict())
+
+
+def test_mx_async_steps_equal_synchronous_steps(lib):
+    """MxShardOptimizer steps enqueued ahead of their found_inf (t and S
+    picked on the device by the previous step's flag) equal the synchronous
+    steps over six steps with skips at steps 2 and 3."""
+    from blockwise_fp8_zero_fold_gb300.optimizer import MxShardOptimizer
+    shapes = [(2, 64, 96), (1, 100, 160)]
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, max_norm=0.5)
+    n = sum(e * r * c for e, r, c in shapes)
+    rng = np.random.default_rng(17)
+    p = torch.from_numpy((rng.standard_normal(n) * 0.02).astype(np.float32)).cuda()
+    gs = [torch.from_numpy((rng.standard_normal(n)).astype(np.float32)).cuda() for _ in range(6)]
+    gs[1][11] = float("inf")
+    gs[2][n - 3] = float("nan")
+    sync = MxShardOptimizer(shapes, loss_scale=1024.0, growth_interval=2, **hp)
+    asy = MxShardOptimizer(shapes, loss_scale=1024.0, growth_interval=2, **hp)
+    for o in (sync, asy):
+        o.master.copy_(p)
+    want = [sync.step(g) for g in gs]
+    got = []
+    for g in gs:
+        got += asy.launch_step_async(g)
+    got += asy.drain()
+    assert want == got == [0, 1, 1, 0, 0, 0]
+    assert (asy.scaler.scale, asy.scaler.step) == (sync.scaler.scale, sync.scaler.step)
+    for name in ("master", "m", "v", "codes", "scales"):
+        assert torch.equal(getattr(sync, name).view(torch.uint8), getattr(asy, name).view(torch.uint8)), name
