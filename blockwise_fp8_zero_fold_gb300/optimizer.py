@@ -16,6 +16,15 @@ follows on its shard [b0, b1):
 Every step of the path runs in libfp8z1.so; this class only owns torch
 buffers and calls the entry points in order.  One process, one GPU: with
 dp_size > 1 the other ranks' norm partials come through ``norm_hook``.
+
+The step loops (same results):
+  step / launch_step + finish_step     one step at a time;
+  launch_step_async + drain            each step enqueued before the previous
+                                       one's found_inf is read (_AsyncSteps);
+  step_from_host (+ finish_host_step)  grads from pinned host memory, FP8
+                                       weights back to it, copies overlapped;
+  capture -> CapturedStep              the step as a CUDA graph.
+MxShardOptimizer runs the MXFP8 variant (one step at a time, or async).
 """
 from __future__ import annotations
 
@@ -55,7 +64,7 @@ class _AsyncSteps:
                 "done": [torch.cuda.Event() for _ in range(2)],
                 "k": 0, "inflight": [],  # slots of unresolved steps, oldest first
             }
-        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        s = self._torch_stream(stream, self.device)
         resolved = []
         while len(st["inflight"]) >= 2:  # resolve step k-2: its flag copy ran long ago
             resolved.append(self._resolve_async())
@@ -88,6 +97,20 @@ class _AsyncSteps:
         # the latest step's accumulators, for stats() once drained
         self.sumsq, self.found_inf = sumsq, found
         return resolved
+
+    @staticmethod
+    def _torch_stream(stream, device):
+        """A torch stream for ``stream`` (None: the current one; a raw
+        cudaStream_t is wrapped)."""
+        if stream is None:
+            return torch.cuda.current_stream(device)
+        return stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(stream)
+
+    def _run_norm_hook(self, stream):
+        """The norm hook (the other ranks' partials), on the step's stream."""
+        if self.norm_hook is not None:
+            with torch.cuda.stream(self._torch_stream(stream, self.device)):
+                self.norm_hook(self.sumsq, self.found_inf)
 
     def _async_busy(self) -> bool:
         st = getattr(self, "_async", None)
@@ -244,8 +267,7 @@ class ShardOptimizer(_AsyncSteps):
             gptrs = self._ptrs(grads)
             F.fp8z1_fold_norm(self.layout, gptrs, None, self.b0, self.b1, self.sumsq, self.found_inf,
                               stream)
-            if self.norm_hook is not None:
-                self.norm_hook(self.sumsq, self.found_inf)
+            self._run_norm_hook(stream)
             # codes go row-major when FP8 params are given, else to the folded buffer
             F.fp8z1_step_fused(self.layout, hp, d_grad_params=gptrs, master_shard=self.master,
                                m_shard=self.m, v_shard=self.v,
@@ -256,8 +278,7 @@ class ShardOptimizer(_AsyncSteps):
             return
         self.fold_into(grads, self.grad, stream)
         F.fp8z1_grad_norm(self.layout, self.grad, self.b0, self.b1, self.sumsq, self.found_inf, stream)
-        if self.norm_hook is not None:
-            self.norm_hook(self.sumsq, self.found_inf)
+        self._run_norm_hook(stream)
         F.fp8z1_step(self.layout, hp, self.grad, self.master, self.m, self.v, self.codes, self.scales,
                      self.b0, self.b1, self.sumsq, self.found_inf, stream)
         if fp8_params is not None:
@@ -614,8 +635,7 @@ class MxShardOptimizer(_AsyncSteps):
         F.fp8z1_norm_reset(self.sumsq, self.found_inf, stream)
         F.fp8z1_mx_grad_norm(self.layout, grad_shard, self.g0, self.g1, self.sumsq, self.found_inf,
                              stream)
-        if self.norm_hook is not None:
-            self.norm_hook(self.sumsq, self.found_inf)
+        self._run_norm_hook(stream)
         hp = F.make_hp(step=self.scaler.step + 1, loss_scale=self.scaler.scale, **self.hp)
         F.fp8z1_mx_step(self.layout, hp, grad_shard, self.master, self.m, self.v, self.codes,
                         self.scales, self.g0, self.g1, self.sumsq, self.found_inf, stream)
