@@ -207,3 +207,69 @@ def test_async_steps_equal_synchronous_steps(lib):
         asy.launch_step_async(g_dev, f_asy)
         asy.step(g_dev, f_asy)
     asy.drain()
+
+
+@pytest.mark.parametrize("mode", ["sync", "async"])
+def test_two_ranks_through_the_norm_hook(lib, mode):
+    """Ranks 0 and 1 of DP = 2 on one GPU: each rank's norm hook adds the
+    other rank's partial sum of squares and ORs its flag, as the all-reduce
+    of "DeepSpeed ZeRO 优化" §七 would, and both write their blocks' codes
+    into the same FP8 weights (the all-gather).  With a nan in rank 1's
+    range on step 2, both ranks skip it.  Their shards and the FP8 weights
+    equal one whole-buffer optimizer's, bit for bit (clipping off: the update
+    does not depend on how the sum was grouped)."""
+    base = dict(shapes=[(3, 512, 384), (1, 1000, 131)], m_sigma=1e-4, v_sigma=1e-8, max_norm=1e30)
+    w1 = synth.workload("tiny", dp=1, rank=0, **base)
+    w2 = synth.workload("tiny", dp=2, rank=0, **base)
+    ref = _make(w1, 0)
+    ranks = [_make(w2, r) for r in (0, 1)]
+    for o in [ref] + ranks:
+        o.init_state(*(synth.make_state(w1, k, "cuda") for k in ("master", "m", "v")))
+    assert ranks[1].b0 <= oracle_block_of_param(w2, 1) < ranks[1].b1
+    fp8_ref = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w1.shapes]
+    fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in w1.shapes]
+    part = torch.zeros(2, dtype=torch.float64, device="cuda")
+    pflag = torch.zeros(2, dtype=torch.int32, device="cuda")
+
+    def hook_for(r):
+        def hook(s, f):  # add the other rank's partial, OR its flag
+            s.add_(part[1 - r:2 - r])
+            torch.maximum(f, pflag[1 - r:2 - r], out=f)
+        return hook
+
+    for r, o in enumerate(ranks):
+        o.norm_hook = hook_for(r)
+    got = [[], []]
+    for t in range(1, 4):
+        g = synth.make_grads(w1, t, "cuda")
+        if t == 2:
+            g[1][0, 5, 7] = float("nan")
+        ref.step(g, fp8_ref)
+        part.zero_()
+        pflag.zero_()
+        for r, o in enumerate(ranks):  # each rank's own partial, as it would send it
+            F.fp8z1_fold_norm(o.layout, F.param_pointers(g), None, o.b0, o.b1, part[r:r + 1], pflag[r:r + 1])
+        for r, o in enumerate(ranks):
+            if mode == "sync":
+                got[r].append(o.step(g, fp8))
+            else:
+                got[r] += o.launch_step_async(g, fp8)
+    if mode == "async":
+        for r, o in enumerate(ranks):
+            got[r] += o.drain()
+    torch.cuda.synchronize()
+    assert got[0] == got[1] == [0, 1, 0]
+    for o in ranks:
+        assert (o.scaler.scale, o.scaler.step) == (ref.scaler.scale, ref.scaler.step) and o.scaler.step == 2
+        sl = slice(o.b0 * 16384, o.b1 * 16384)
+        for name in ("master", "m", "v"):
+            assert torch.equal(getattr(o, name).view(torch.int32), getattr(ref, name)[sl].view(torch.int32)), name
+        assert torch.equal(o.scales, ref.scales[o.b0:o.b1])
+    for a, b in zip(fp8, fp8_ref):
+        assert torch.equal(a, b)
+
+
+def oracle_block_of_param(w, p):
+    """The first block of param p in the workload's block order."""
+    import oracle
+    return oracle.count_blocks(w.shapes[:p])
