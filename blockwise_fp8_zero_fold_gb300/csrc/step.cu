@@ -7,6 +7,7 @@
 // and their scales; "DeepSpeed ZeRO 优化" §三 / §六 / §七: unscale and clip,
 // then the update; a found inf skips the step.
 #include <algorithm>
+#include <vector>
 
 #include "step_args.h"
 
@@ -191,6 +192,64 @@ extern "C" int fp8z1_step_fused_select(const fp8z1_layout* L, const fp8z1_adamw_
     return step_fused_impl(L, hp_if_clear, hp_if_set, d_select, nullptr, nullptr, grad_shard, d_grad_params,
                            master_shard, m_shard, v_shard, fp8_shard, d_fp8_params, scale_shard, nullptr, nullptr,
                            b0, b1, d_sumsq, d_found_inf, stream);
+}
+
+extern "C" int fp8z1_graph_step_nodes(void* graph, void** nodes, int32_t capacity, int32_t* n_nodes)
+{
+    if (!graph || !n_nodes || capacity < 0 || (capacity > 0 && !nodes)) return FP8Z1_EINVAL;
+    cudaGraph_t g = static_cast<cudaGraph_t>(graph);
+    size_t n = 0;
+    if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    std::vector<cudaGraphNode_t> all(n);
+    if (n && cudaGraphGetNodes(g, all.data(), &n) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    int32_t found = 0;
+    for (cudaGraphNode_t node : all) {
+        cudaGraphNodeType type;
+        if (cudaGraphNodeGetType(node, &type) != cudaSuccess || type != cudaGraphNodeTypeKernel) continue;
+        cudaKernelNodeParams kp = {};
+        if (cudaGraphKernelNodeGetParams(node, &kp) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (!is_value_kernel<false>(kp.func) && !is_value_kernel<true>(kp.func)) continue;
+        if (found < capacity) nodes[found] = node;
+        ++found;
+    }
+    *n_nodes = found;
+    return found > capacity ? FP8Z1_EINVAL : FP8Z1_OK;
+}
+
+extern "C" int fp8z1_graph_set_step_hp(void* graph_exec, void* const* nodes, int32_t n_nodes,
+                                       const fp8z1_adamw_hp* hp)
+{
+    if (!graph_exec || n_nodes < 0 || (n_nodes > 0 && !nodes) || !hp || !in_domain(hp)) return FP8Z1_EINVAL;
+    cudaGraphExec_t exec = static_cast<cudaGraphExec_t>(graph_exec);
+    const StepScalars c = scalars(hp);
+    for (int32_t i = 0; i < n_nodes; ++i) {
+        cudaGraphNode_t node = static_cast<cudaGraphNode_t>(nodes[i]);
+        cudaKernelNodeParams kp = {};
+        if (cudaGraphKernelNodeGetParams(node, &kp) != cudaSuccess || !kp.kernelParams ||
+            (!is_value_kernel<false>(kp.func) && !is_value_kernel<true>(kp.func))) {
+            cudaGetLastError();
+            return FP8Z1_EINVAL;
+        }
+        StepArgs a = *static_cast<const StepArgs*>(kp.kernelParams[0]);
+        a.c = c;
+        void* args[] = {&a};
+        kp.kernelParams = args;
+        kp.extra = nullptr;
+        if (cudaGraphExecKernelNodeSetParams(exec, node, &kp) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8Z1_ECUDA;
+        }
+    }
+    return FP8Z1_OK;
 }
 
 extern "C" int fp8z1_step_scalars_from_hp(const fp8z1_adamw_hp* hp, fp8z1_step_scalars* out)

@@ -56,5 +56,13 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms);
 extern template void launch<false>(const StepArgs&, int64_t, cudaStream_t, unsigned);
 extern template void launch<true>(const StepArgs&, int64_t, cudaStream_t, unsigned);
 
+// Whether `func` is one of the step kernels taking its scalars by value (the
+// ones whose captured graph nodes fp8z1_graph_set_step_hp may rewrite).
+template <bool PAD>
+bool is_value_kernel(const void* func);
+
+extern template bool is_value_kernel<false>(const void*);
+extern template bool is_value_kernel<true>(const void*);
+
 }  // namespace stepk
 }  // namespace fp8z1

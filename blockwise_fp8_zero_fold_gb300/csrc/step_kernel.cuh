@@ -311,5 +311,22 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
 #undef FP8Z1_STEP_FORM
 }
 
+template <bool PAD>
+bool is_value_kernel(const void* func)
+{
+#define FP8Z1_STEP_VALUE_FORM(GR, CR, CF, MON) \
+    if (func == reinterpret_cast<const void*>(&step_kernel<GR, CR, CF, MON, kScValue, PAD>)) return true;
+#define FP8Z1_STEP_VALUE_FORMS(GR, CR, CF) FP8Z1_STEP_VALUE_FORM(GR, CR, CF, false) FP8Z1_STEP_VALUE_FORM(GR, CR, CF, true)
+    FP8Z1_STEP_VALUE_FORMS(true, true, true)
+    FP8Z1_STEP_VALUE_FORMS(true, true, false)
+    FP8Z1_STEP_VALUE_FORMS(true, false, true)
+    FP8Z1_STEP_VALUE_FORMS(false, true, true)
+    FP8Z1_STEP_VALUE_FORMS(false, true, false)
+    FP8Z1_STEP_VALUE_FORMS(false, false, true)
+#undef FP8Z1_STEP_VALUE_FORMS
+#undef FP8Z1_STEP_VALUE_FORM
+    return false;
+}
+
 }  // namespace stepk
 }  // namespace fp8z1

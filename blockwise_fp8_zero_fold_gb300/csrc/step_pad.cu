@@ -2,3 +2,4 @@
 #include "step_kernel.cuh"
 
 template void fp8z1::stepk::launch<true>(const fp8z1::stepk::StepArgs&, int64_t, cudaStream_t, unsigned);
+template bool fp8z1::stepk::is_value_kernel<true>(const void*);

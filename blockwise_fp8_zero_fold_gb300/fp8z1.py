@@ -90,6 +90,8 @@ _SIGS = {
                                        C.c_int64, C.c_int64, _P, _P, _P]),
     "fp8z1_step_fused_select": (C.c_int, [_P, C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_adamw_hp), _P, _P, _P,
                                           _P, _P, _P, _P, _P, _P, C.c_int64, C.c_int64, _P, _P, _P]),
+    "fp8z1_graph_step_nodes": (C.c_int, [_P, _P, C.c_int32, C.POINTER(C.c_int32)]),
+    "fp8z1_graph_set_step_hp": (C.c_int, [_P, _P, C.c_int32, C.POINTER(fp8z1_adamw_hp)]),
     "fp8z1_step_scalars_from_hp": (C.c_int, [C.POINTER(fp8z1_adamw_hp), C.POINTER(fp8z1_step_scalars)]),
     "fp8z1_paramwise_split": (C.c_int, [C.POINTER(fp8z1_shape), C.c_int32, C.c_int32, _P, _P,
                                         C.POINTER(C.c_int64)]),
@@ -323,6 +325,25 @@ def fp8z1_step_fused_select(layout: Layout, hp_if_clear: fp8z1_adamw_hp, hp_if_s
                                          _ptr(v_shard), _ptr(fp8_shard), _ptr(d_fp8_params), _ptr(scale_shard),
                                          int(b0), int(b1), _ptr(d_sumsq), _ptr(d_found_inf), _stream(stream)),
            "fp8z1_step_fused_select")
+
+
+def fp8z1_graph_step_nodes(graph: int):
+    """The by-value step kernel nodes of a captured cudaGraph_t, as a ctypes
+    array of node handles."""
+    n = C.c_int32()
+    st = lib().fp8z1_graph_step_nodes(C.c_void_p(graph), None, 0, C.byref(n))
+    if st not in (OK, EINVAL) or (st == EINVAL and n.value == 0):
+        _check(st, "fp8z1_graph_step_nodes")
+    nodes = (C.c_void_p * max(1, n.value))()
+    _check(lib().fp8z1_graph_step_nodes(C.c_void_p(graph), C.cast(nodes, C.c_void_p), n.value, C.byref(n)),
+           "fp8z1_graph_step_nodes")
+    return nodes, n.value
+
+
+def fp8z1_graph_set_step_hp(graph_exec: int, nodes, n_nodes: int, hp: fp8z1_adamw_hp):
+    """Rewrite the step scalars of those nodes in a cudaGraphExec_t."""
+    _check(lib().fp8z1_graph_set_step_hp(C.c_void_p(graph_exec), C.cast(nodes, C.c_void_p), int(n_nodes),
+                                         C.byref(hp)), "fp8z1_graph_set_step_hp")
 
 
 def fp8z1_step_scalars_from_hp(hp: fp8z1_adamw_hp, out=None) -> fp8z1_step_scalars:

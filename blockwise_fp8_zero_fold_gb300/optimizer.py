@@ -455,10 +455,10 @@ class ShardOptimizer(_AsyncSteps):
         return self.finish_step()
 
     def capture(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]] = None,
-                pool=None, slots: int = 2) -> "CapturedStep":
+                pool=None, slots: int = 2, mode: str = "auto") -> "CapturedStep":
         """Capture one fused step over these grad (and FP8 weight) tensors in a
         CUDA graph; see ``CapturedStep``."""
-        return CapturedStep(self, grads, fp8_params, pool, slots)
+        return CapturedStep(self, grads, fp8_params, pool, slots, mode)
 
     def stats(self, loss_scale: Optional[float] = None) -> dict:
         """Numbers for logging the last step (reads two device scalars): the
@@ -494,23 +494,40 @@ class CapturedStep:
     """One fused step of a ``ShardOptimizer`` as a CUDA graph: zero the norm
     accumulators, the norm read from the row-major grads (then the norm hook,
     which is captured too, so it must be capturable: an NCCL all-reduce is),
-    a copy of the step's scalars from page-locked host memory, and the step
-    reading them from device memory (fp8z1_step_fused_dev).  A replay thus
-    costs one graph launch however many entry points the step has.
+    and the step.  A replay costs one graph launch however many entry points
+    the step has.
+
+    t and S change every step, so the graph cannot replay the scalars it was
+    captured with.  Two ways of feeding it this step's:
+      "patch"  the step is the by-value kernel (fp8z1_step_fused), and before
+               each replay its scalars are rewritten in the instantiated graph
+               (fp8z1_graph_set_step_hp): the kernel runs at full speed.
+               Needs torch's raw graph handles (CUDAGraph(keep_graph=True)).
+      "device" the step reads its scalars from device memory, copied in the
+               graph from a pinned slot that ``replay`` rewrites
+               (fp8z1_step_fused_dev); the kernel holds the scalars in
+               registers and runs a few per cent slower.  The step is captured
+               ``slots`` times, each graph copying from its own slot and
+               replayed in turn, so the host can enqueue step k+1 before step
+               k's copy of its scalars has run.
+    "auto" takes "patch" when torch offers it.
 
     The graph holds the addresses of the tensors it was captured with: each
     step, write the new grads into those same ``grads`` tensors, and read the
-    FP8 weights from those ``fp8_params`` (or ``codes`` when None).  t and S
-    live on the host as before: ``replay`` writes this step's scalars to the
-    pinned slot its graph copies from; ``step`` also reads found_inf and
-    updates the loss scaler, like ``ShardOptimizer.step``.  The step is
-    captured ``slots`` times, each graph copying from its own pinned slot and
-    replayed in turn, so the host can enqueue step k+1 before step k's copy of
-    its scalars has run."""
+    FP8 weights from those ``fp8_params`` (or ``codes`` when None).  t, S and
+    the other hyper-parameters are the optimizer's when ``replay`` runs (a
+    schedule may change lr); ``step`` also reads found_inf and updates the
+    loss scaler, like ``ShardOptimizer.step``."""
 
-    def __init__(self, opt: "ShardOptimizer", grads, fp8_params=None, pool=None, slots: int = 2):
+    def __init__(self, opt: "ShardOptimizer", grads, fp8_params=None, pool=None, slots: int = 2,
+                 mode: str = "auto"):
         if not opt.fused:
             raise ValueError("a captured step runs the fused path")
+        if mode == "auto":
+            mode = "patch" if self.patch_supported() else "device"
+        if mode not in ("patch", "device"):
+            raise ValueError(f"unknown mode {mode!r}")
+        self.mode = mode
         self.opt = opt
         self.grads = list(grads)
         self.fp8_params = None if fp8_params is None else list(fp8_params)
@@ -518,22 +535,35 @@ class CapturedStep:
         self._gptrs = opt._ptrs(self.grads)
         self._fptrs = None if fp8_params is None else opt._ptrs(self.fp8_params)
         nsc = C.sizeof(F.fp8z1_step_scalars) // 4
-        self._h = [torch.zeros(nsc, dtype=torch.float32, pin_memory=True) for _ in range(slots)]
+        n_slots = slots if mode == "device" else 0
+        self._h = [torch.zeros(nsc, dtype=torch.float32, pin_memory=True) for _ in range(n_slots)]
         self._d = torch.zeros(nsc, dtype=torch.float32, device=opt.device)
-        self._done = [torch.cuda.Event() for _ in range(slots)]
+        self._done = [torch.cuda.Event() for _ in range(n_slots)]
         self._next = 0
         # load every kernel once outside the capture: found_inf preset makes
         # the step a no-op, and the accumulators are zeroed in the graph
         side = torch.cuda.Stream(opt.device)
         side.wait_stream(torch.cuda.current_stream(opt.device))
         with torch.cuda.stream(side):
-            self._write(self._h[0])
+            if mode == "device":
+                self._write(self._h[0])
             opt.found_inf.fill_(1)
-            self._enqueue(self._h[0], norm_hook=False)
+            self._enqueue(self._h[0] if mode == "device" else None, norm_hook=False)
             F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
         side.synchronize()
         torch.cuda.current_stream(opt.device).wait_stream(side)
         self.graphs = []
+        if mode == "patch":
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+            with torch.cuda.graph(g, pool=pool, stream=side):  # nothing is allocated inside
+                F.fp8z1_norm_reset(opt.sumsq, opt.found_inf)
+                self._enqueue(None, norm_hook=True)
+            g.instantiate()
+            self.graphs.append(g)
+            self._nodes, self._n_nodes = F.fp8z1_graph_step_nodes(g.raw_cuda_graph())
+            if self._n_nodes == 0:
+                raise RuntimeError("no step kernel found in the captured graph")
+            return
         for h in self._h:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, pool=pool, stream=side):  # nothing is allocated inside
@@ -541,28 +571,48 @@ class CapturedStep:
                 self._enqueue(h, norm_hook=True)
             self.graphs.append(g)
 
+    @staticmethod
+    def patch_supported() -> bool:
+        """Whether torch exposes the raw graph handles the "patch" mode needs."""
+        try:
+            torch.cuda.CUDAGraph(keep_graph=True)
+        except TypeError:
+            return False
+        return hasattr(torch.cuda.CUDAGraph, "raw_cuda_graph") and hasattr(torch.cuda.CUDAGraph,
+                                                                          "raw_cuda_graph_exec")
+
+    def _hp(self):
+        o = self.opt
+        return F.make_hp(step=o.scaler.step + 1, loss_scale=o.scaler.scale, **o.hp)
+
     def _write(self, h: torch.Tensor):
         """This step's scalars into pinned slot ``h``: t and S from the scaler,
         the rest from ``opt.hp`` as it is now (a schedule may change lr)."""
-        o = self.opt
-        F.fp8z1_step_scalars_from_hp(F.make_hp(step=o.scaler.step + 1, loss_scale=o.scaler.scale, **o.hp), h)
+        F.fp8z1_step_scalars_from_hp(self._hp(), h)
 
     def _enqueue(self, h, norm_hook: bool):
         o = self.opt
         F.fp8z1_fold_norm(o.layout, self._gptrs, None, o.b0, o.b1, o.sumsq, o.found_inf)
         if norm_hook and o.norm_hook is not None:
             o.norm_hook(o.sumsq, o.found_inf)
-        F.fp8z1_step_fused_dev(o.layout, h, self._d, d_grad_params=self._gptrs,
-                               master_shard=o.master, m_shard=o.m, v_shard=o.v,
-                               fp8_shard=o.codes if self._fptrs is None else None, d_fp8_params=self._fptrs,
-                               scale_shard=o.scales, b0=o.b0, b1=o.b1, d_sumsq=o.sumsq,
-                               d_found_inf=o.found_inf)
+        kw = dict(d_grad_params=self._gptrs, master_shard=o.master, m_shard=o.m, v_shard=o.v,
+                  fp8_shard=o.codes if self._fptrs is None else None, d_fp8_params=self._fptrs,
+                  scale_shard=o.scales, b0=o.b0, b1=o.b1, d_sumsq=o.sumsq, d_found_inf=o.found_inf)
+        if h is None:
+            F.fp8z1_step_fused(o.layout, self._hp(), **kw)
+        else:
+            F.fp8z1_step_fused_dev(o.layout, h, self._d, **kw)
 
     def replay(self):
-        """Enqueue one step on the current stream (no host synchronisation,
-        unless this slot's previous replay has not finished).  t and S are
-        the scaler's when the step is enqueued: ``finish_step`` between
-        replays advances them, as with ``ShardOptimizer.launch_step``."""
+        """Enqueue one step on the current stream (in "device" mode, no host
+        synchronisation unless this slot's previous replay has not finished).
+        t and S are the scaler's when the step is enqueued: ``finish_step``
+        between replays advances them, as with ``ShardOptimizer.launch_step``."""
+        if self.mode == "patch":
+            g = self.graphs[0]
+            F.fp8z1_graph_set_step_hp(g.raw_cuda_graph_exec(), self._nodes, self._n_nodes, self._hp())
+            g.replay()
+            return
         k = self._next
         self._next = (k + 1) % len(self.graphs)
         self._done[k].synchronize()  # its pinned scalars are about to be overwritten

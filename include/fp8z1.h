@@ -289,6 +289,24 @@ int fp8z1_step_fused(const fp8z1_layout* layout, const fp8z1_adamw_hp* hp, const
                      float* scale_shard, float* block_cos, uint32_t* block_underflow, int64_t b0,
                      int64_t b1, const double* d_sumsq, const int32_t* d_found_inf, void* stream);
 
+/* ---- re-targeting a captured step (CUDA graphs, scalars by value) ----------- */
+
+/* The step kernels of this library that take their scalars by value
+ * (those of fp8z1_step and fp8z1_step_fused) inside a captured CUDA graph `graph` (a cudaGraph_t): up to
+ * `capacity` node handles (cudaGraphNode_t) go to `nodes`, their count to
+ * *n_nodes.  Host only; EINVAL when there are more than `capacity` (n_nodes
+ * then holds the count), ECUDA when the graph cannot be read. */
+int fp8z1_graph_step_nodes(void* graph, void** nodes, int32_t capacity, int32_t* n_nodes);
+
+/* Rewrite the per-step scalars (t, S and the rest, from *hp, formed as
+ * fp8z1_step forms them) of those nodes in the instantiated graph
+ * `graph_exec` (a cudaGraphExec_t of `graph`): the next launches of the
+ * graph run the step with *hp, at the speed of the by-value kernel; launches
+ * already made are unaffected.  Each node's other arguments stay as
+ * captured.  Host only; EINVAL (a node is not one of this library's step
+ * kernels, hp out of domain), ECUDA. */
+int fp8z1_graph_set_step_hp(void* graph_exec, void* const* nodes, int32_t n_nodes, const fp8z1_adamw_hp* hp);
+
 /* ---- the step with two candidate hyper-parameter sets ------------------------ */
 
 /* fp8z1_step_fused (without monitors) taking two hyper-parameter sets, both by

@@ -14,6 +14,10 @@
  *                                  same grads) replayed from one CUDA graph:
  *                                  zero the accumulators, norm, copy of the
  *                                  step scalars from pinned memory, step
+ *   c_abi_example graph_patch <in> <out>  the same three steps from one graph
+ *                                  of the by-value step, whose scalars are
+ *                                  rewritten in the executable graph before
+ *                                  each launch (fp8z1_graph_set_step_hp)
  */
 #include <cuda_runtime.h>
 #include <stdio.h>
@@ -72,7 +76,7 @@ static int host_part(void)
 }
 
 static int gpu_part(const char* in, const char* out, int graph)
-{
+{ /* graph: 0 none, 1 device scalars, 2 patched */
     const int64_t R = 300, C = 200, n_real = R * C, nblk = 6, n = nblk * FP8Z1_BLOCK_ELEMS;
     float* h = (float*)malloc(sizeof(float) * 2 * n_real);
     FILE* f = fopen(in, "rb");
@@ -112,6 +116,31 @@ static int gpu_part(const char* in, const char* out, int graph)
         CHECK(fp8z1_step_fused(L, &hp, NULL, (const float* const*)&d_ptrs[1], d_master, d_m, d_v, NULL,
                                (uint8_t* const*)&d_ptrs[2], d_scales, NULL, NULL, 0, nblk, d_sumsq, d_found,
                                NULL));
+    } else if (graph == 2) {
+        cudaStream_t st;
+        cudaGraph_t g;
+        cudaGraphExec_t ge;
+        void* nodes[4];
+        int32_t n_nodes = 0;
+        CUDA(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+        CUDA(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+        CHECK(fp8z1_norm_reset(d_sumsq, d_found, st));
+        CHECK(fp8z1_fold_norm(L, (const float* const*)&d_ptrs[1], NULL, 0, nblk, d_sumsq, d_found, st));
+        CHECK(fp8z1_step_fused(L, &hp, NULL, (const float* const*)&d_ptrs[1], d_master, d_m, d_v, NULL,
+                               (uint8_t* const*)&d_ptrs[2], d_scales, NULL, NULL, 0, nblk, d_sumsq, d_found, st));
+        CUDA(cudaStreamEndCapture(st, &g));
+        CUDA(cudaGraphInstantiate(&ge, g, 0));
+        CHECK(fp8z1_graph_step_nodes(g, nodes, 4, &n_nodes));
+        if (n_nodes != 1) return 1;
+        for (int64_t t = 1; t <= 3; ++t) {
+            hp.step = t;
+            CHECK(fp8z1_graph_set_step_hp(ge, nodes, n_nodes, &hp));
+            CUDA(cudaGraphLaunch(ge, st));
+        }
+        CUDA(cudaStreamSynchronize(st));
+        CUDA(cudaGraphExecDestroy(ge));
+        CUDA(cudaGraphDestroy(g));
+        CUDA(cudaStreamDestroy(st));
     } else {
         fp8z1_step_scalars *h_sc, *d_sc;
         cudaStream_t st;
@@ -165,6 +194,7 @@ int main(int argc, char** argv)
     if (argc >= 2 && strcmp(argv[1], "host") == 0) return host_part();
     if (argc >= 4 && strcmp(argv[1], "gpu") == 0) return gpu_part(argv[2], argv[3], 0);
     if (argc >= 4 && strcmp(argv[1], "graph") == 0) return gpu_part(argv[2], argv[3], 1);
-    fprintf(stderr, "usage: %s host | gpu <in> <out> | graph <in> <out>\n", argv[0]);
+    if (argc >= 4 && strcmp(argv[1], "graph_patch") == 0) return gpu_part(argv[2], argv[3], 2);
+    fprintf(stderr, "usage: %s host | gpu|graph|graph_patch <in> <out>\n", argv[0]);
     return 2;
 }

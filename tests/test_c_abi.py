@@ -50,10 +50,11 @@ def test_host_calls_from_c(exe):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("mode,steps", [("gpu", 1), ("graph", 3)])
+@pytest.mark.parametrize("mode,steps", [("gpu", 1), ("graph", 3), ("graph_patch", 3)])
 def test_steps_from_c(exe, tmp_path, mode, steps):
-    """One step, or three replays of one captured graph (t = 1, 2, 3 written
-    to pinned memory between them), from plain C against the oracle."""
+    """One step, or three launches of one captured graph (t = 1, 2, 3 written
+    to pinned memory between them, or patched into the executable graph's
+    step node), from plain C against the oracle."""
     rng = np.random.default_rng(31)
     g = (rng.standard_normal((300, 200)) * 1024e-3).astype(np.float32)
     p = (rng.standard_normal((300, 200)) * 0.02).astype(np.float32)

@@ -120,7 +120,8 @@ def _oracle_steps(gsteps, ph, loss_scale0, growth):
     return op, om, ov, q, scales, found, sc
 
 
-def test_captured_steps_match_oracle(lib):
+@pytest.mark.parametrize("mode", ["patch", "device"])
+def test_captured_steps_match_oracle(lib, mode):
     """Four steps through one captured graph, the third with a nan grad (a
     skipped step: S halves, t stays) and the learning rate halved before the
     fourth: master, m, v, scales and the row-major codes match the oracle's
@@ -142,13 +143,18 @@ def test_captured_steps_match_oracle(lib):
     op, om, ov, q, oscales, found, osc = _oracle_steps(scaled, ph, scale0, growth)
     assert found == [0, 0, 1, 0]
 
+    from blockwise_fp8_zero_fold_gb300.optimizer import CapturedStep
+    if mode == "patch" and not CapturedStep.patch_supported():
+        pytest.skip("this torch has no raw CUDA graph handles")
     runs = {}
-    for mode in ("graph", "eager"):
+    for run in ("graph", "eager"):
         opt = ShardOptimizer(SHAPES, loss_scale=scale0, growth_interval=growth, **HP)
         opt.init_state(_dev(ph))
         grads = [torch.zeros(s, device="cuda") for s in SHAPES]
         fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in SHAPES]
-        cap = opt.capture(grads, fp8) if mode == "graph" else None
+        cap = opt.capture(grads, fp8, mode=mode) if run == "graph" else None
+        if cap is not None:
+            assert cap.mode == mode
         got = []
         for k, gh in enumerate(scaled):
             if k == 3:
@@ -159,11 +165,11 @@ def test_captured_steps_match_oracle(lib):
         torch.cuda.synchronize()
         assert got == found
         assert (opt.scaler.scale, opt.scaler.step) == (osc.scale, osc.step)
-        runs[mode] = (opt, fp8)
-        assert_rel(to_host(opt.master), op, 1e-6, f"{mode} master")
-        assert_rel(to_host(opt.m), om, 1e-6, f"{mode} m")
-        assert_rel(to_host(opt.v), ov, 1e-6, f"{mode} v")
-        assert_rel(to_host(opt.scales), oscales, 1e-6, f"{mode} scales")
+        runs[run] = (opt, fp8)
+        assert_rel(to_host(opt.master), op, 1e-6, f"{run} master")
+        assert_rel(to_host(opt.m), om, 1e-6, f"{run} m")
+        assert_rel(to_host(opt.v), ov, 1e-6, f"{run} v")
+        assert_rel(to_host(opt.scales), oscales, 1e-6, f"{run} scales")
         want = [np.zeros(s, np.uint8) for s in SHAPES]
         oracle.unfold(SHAPES, q, want)
         for a, b in zip(fp8, want):
