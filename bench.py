@@ -220,7 +220,7 @@ def bench_ours(args, rank, world, dist):
             # the kernel picks t and S by that flag, the host reads it a step late
             for i in range(k):
                 ev = None if events is None else {"norm": events["fold_norm"][i], "step": events["step"][i]}
-                skipped += sum(opt.launch_step_async(grads, fp8, stream, ev))
+                skipped += sum(opt.launch_step_async(gptrs, fptrs, stream, ev))
             return skipped + sum(opt.drain())
         for i in range(k):
             for name, fn in stages(path):

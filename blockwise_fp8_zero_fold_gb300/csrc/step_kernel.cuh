@@ -146,6 +146,9 @@ template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, int SC, 
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
+    if (SC == kScGateClear || SC == kScGateSet) {
+        if ((*a.select != 0) != (SC == kScGateSet)) return;  // the other set's launch does the step
+    }
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
     __shared__ StepScalars s_c;
@@ -291,16 +294,22 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
 #define FP8Z1_STEP_FORM(GR, CR, CF, MON, SCAL)                                                       \
     if (forms == ((GR ? kGradRows : 0u) | (CR ? kCodesRows : 0u) | (CF ? kCodesFolded : 0u) |         \
                   (MON ? kMonitors : 0u) | (SCAL == kScDevice ? kDevScalars : 0u) |                   \
-                  (SCAL == kScSelect ? kSelScalars : 0u))) {                                         \
+                  (SCAL == kScSelect ? kSelScalars : 0u) | (SCAL == kScGateClear ? kGateClear : 0u) |  \
+                  (SCAL == kScGateSet ? kGateSet : 0u))) {                                           \
         step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, 0, s>>>(a);                \
         return;                                                                                      \
     }
 #define FP8Z1_STEP_FORMS_GC(GR, CR, CF)                                                              \
     FP8Z1_STEP_FORM(GR, CR, CF, false, kScValue)                                                     \
     FP8Z1_STEP_FORM(GR, CR, CF, false, kScDevice)                                                    \
-    FP8Z1_STEP_FORM(GR, CR, CF, false, kScSelect)                                                    \
     FP8Z1_STEP_FORM(GR, CR, CF, true, kScValue)                                                      \
-    FP8Z1_STEP_FORM(GR, CR, CF, true, kScDevice)
+    FP8Z1_STEP_FORM(GR, CR, CF, true, kScDevice)                                                     \
+    if (!PAD) {                                                                                      \
+        FP8Z1_STEP_FORM(GR, CR, CF, false, kScSelect)                                                \
+    } else {                                                                                         \
+        FP8Z1_STEP_FORM(GR, CR, CF, false, kScGateClear)                                             \
+        FP8Z1_STEP_FORM(GR, CR, CF, false, kScGateSet)                                               \
+    }
     FP8Z1_STEP_FORMS_GC(true, true, true)
     FP8Z1_STEP_FORMS_GC(true, true, false)
     FP8Z1_STEP_FORMS_GC(true, false, true)

@@ -176,8 +176,20 @@ class ShardOptimizer(_AsyncSteps):
     # -- pointer arrays for fold/unfold ------------------------------------
     _PTR_CACHE = 16  # distinct tensor sets whose device pointer arrays are kept
 
-    def _ptrs(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
-        """Device array of the tensors' data pointers (cached per tensor set)."""
+    def pointers(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
+        """The device array of the params' data pointers that the step calls
+        read.  A step loop over the same tensors can pass it instead of the
+        tensor list, which spares the per-call check of every tensor (it
+        matters with thousands of params)."""
+        return self._ptrs(tensors)
+
+    def _ptrs(self, tensors) -> torch.Tensor:
+        """Device array of the tensors' data pointers (cached per tensor set);
+        a device int64 array of n_params pointers passes through."""
+        if isinstance(tensors, torch.Tensor):
+            if tensors.dtype != torch.int64 or tensors.numel() != len(self.shapes) or tensors.device.type != "cuda":
+                raise ValueError("a pointer array must be a device int64 tensor with one entry per param")
+            return tensors
         if len(tensors) != len(self.shapes):
             raise ValueError(f"expected {len(self.shapes)} tensors, got {len(tensors)}")
         for t, shp in zip(tensors, self.shapes):
@@ -415,11 +427,11 @@ class ShardOptimizer(_AsyncSteps):
         return found
 
     # -- steps enqueued ahead of their found_inf --------------------------------
-    def launch_step_async(self, grads: Sequence[torch.Tensor], fp8_params: Optional[Sequence[torch.Tensor]],
-                          stream=None, events: Optional[dict] = None) -> List[int]:
+    def launch_step_async(self, grads, fp8_params, stream=None, events: Optional[dict] = None) -> List[int]:
         """Enqueue one fused step without waiting for the previous one
-        (``_AsyncSteps``; fp8z1_step_fused_select).  Returns the found_inf of
-        the steps resolved by this call, oldest first; ``drain`` resolves the
+        (``_AsyncSteps``; fp8z1_step_fused_select).  ``grads`` / ``fp8_params``:
+        the param tensors or their ``pointers``.  Returns the found_inf of the
+        steps resolved by this call, oldest first; ``drain`` resolves the
         rest.  ``events``: optional {"norm": (start, end), "step": (start,
         end)} CUDA events to record around the two kernels on ``stream``."""
         if not self.fused:

@@ -60,7 +60,9 @@ def test_bench_line_tiny():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["other_path"]["path"] == "unfused"
-    assert d["gpu_launches"] == 2 * 4  # the flat-run norm and one step launch per step
+    # per step: the flat-run norm, and the step (one launch; two gated ones for a
+    # padded run when the step picks its scalars by the previous step's flag)
+    assert 2 * 4 <= d["gpu_launches"] <= 3 * 4
 
 
 @pytest.mark.gpu

@@ -190,10 +190,11 @@ def test_async_steps_equal_synchronous_steps(lib):
     want = [sync.step(g, f_sync) for g in gs]
     got = []
     g_dev = [torch.empty_like(x) for x in gs[0]]
+    g_ptrs, f_ptrs = asy.pointers(g_dev), asy.pointers(f_asy)  # the loop passes pointer arrays
     for g in gs:
         for d, x in zip(g_dev, g):
             d.copy_(x)  # the same grad tensors every step, refilled in stream order
-        got += asy.launch_step_async(g_dev, f_asy)
+        got += asy.launch_step_async(g_ptrs, f_ptrs)
     got += asy.drain()
     assert want == got == [int(t in bad) for t in range(1, 9)]
     assert (asy.scaler.scale, asy.scaler.step, asy.scaler.good_steps) == \
