@@ -251,7 +251,8 @@ def bench_ours(args, rank, world, dist):
         torch.cuda.synchronize()
         ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
         kern = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in names}
-        return ms, kern, sk, launches
+        kern_med = {n: statistics.median(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+        return ms, kern, sk, launches, kern_med
 
     gptrs = opt._ptrs(grads)
     fptrs = opt._ptrs(fp8)
@@ -264,7 +265,7 @@ def bench_ours(args, rank, world, dist):
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    elapsed_ms, kern, skipped, launches = timed(args.path, args.steps)
+    elapsed_ms, kern, skipped, launches, kern_med = timed(args.path, args.steps)
     clk = clocks.stop()
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(n_pad, world, args.steps, elapsed_ms / 1e3)
@@ -272,7 +273,7 @@ def bench_ours(args, rank, world, dist):
     if args.compare:
         alt = "unfused" if args.path == "fused" else "fused"
         run_steps(alt, 2)
-        a_ms, a_kern, _, _ = timed(alt, max(3, args.steps // 4))
+        a_ms, a_kern, _, _, _ = timed(alt, max(3, args.steps // 4))
         other = {"path": alt, "ms_per_step": a_ms / max(3, args.steps // 4), "kernels_ms": a_kern}
     if gbuf is not None:
         del gbuf
@@ -387,6 +388,8 @@ def bench_ours(args, rank, world, dist):
         "kernels_gbs": gbs,
         "other_path": other,
         "step_kernel_elem_per_s": n_pad / (kern["step"] / 1e3),
+        "kernels_ms_median": kern_med,
+        "real_elem_per_s": whole_job_rate(n_real, world, args.steps, elapsed_ms / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": ("fp8z1_step_fused_select" if args.pipeline else "fp8z1_step_fused")
