@@ -180,3 +180,40 @@ def test_captured_steps_match_oracle(lib, mode):
         assert torch.equal(getattr(ga, name).view(torch.int32), getattr(gb, name).view(torch.int32))
     for a, b in zip(f8a, f8b):
         assert torch.equal(a, b)
+
+
+def test_patched_graph_with_several_step_launches(lib):
+    """A layout whose full-tile run sits between padded params captures three
+    step launches (padded, full tiles, padded); fp8z1_graph_step_nodes finds
+    all three (and reports the count when the caller's array is short), and
+    the patched graph replays two steps equal to the eager path."""
+    from blockwise_fp8_zero_fold_gb300.optimizer import CapturedStep
+    if not CapturedStep.patch_supported():
+        pytest.skip("this torch has no raw CUDA graph handles")
+    shapes = [(1, 300, 200), (1, 2560, 3840), (2, 129, 257)]
+    rng = np.random.default_rng(29)
+    ph = [(rng.standard_normal(s) * 0.02).astype(np.float32) for s in shapes]
+    runs = {}
+    for run in ("graph", "eager"):
+        opt = ShardOptimizer(shapes, loss_scale=1024.0, growth_interval=1000, **HP)
+        opt.init_state(_dev(ph))
+        grads = [torch.zeros(s, device="cuda") for s in shapes]
+        fp8 = [torch.zeros(s, dtype=torch.uint8, device="cuda") for s in shapes]
+        cap = opt.capture(grads, fp8, mode="patch") if run == "graph" else None
+        if cap is not None:
+            assert cap._n_nodes == 3
+            n = C.c_int32()
+            g = cap.graphs[0].raw_cuda_graph()
+            assert F.lib().fp8z1_graph_step_nodes(C.c_void_p(g), None, 0, C.byref(n)) == F.EINVAL and n.value == 3
+        r = np.random.default_rng(3)
+        for _ in range(2):
+            for t, s in zip(grads, shapes):
+                t.copy_(torch.from_numpy((r.standard_normal(s) * 1024e-3).astype(np.float32)))
+            assert (cap.step() if cap else opt.step(grads, fp8)) == 0
+        torch.cuda.synchronize()
+        runs[run] = (opt, fp8)
+    (a, fa), (b, fb) = runs["graph"], runs["eager"]
+    for name in ("master", "m", "v", "scales"):
+        assert torch.equal(getattr(a, name).view(torch.int32), getattr(b, name).view(torch.int32)), name
+    for x, y in zip(fa, fb):
+        assert torch.equal(x, y)
