@@ -24,7 +24,9 @@
  *     block b0 of its buffer and holds (b1 - b0) * 16384 elements
  *     (scale_shard: b1 - b0 floats).  Shard pointers must be 16-byte aligned.
  *   - The caller owns every device buffer it passes; the library owns only the
- *     layout (host tables, the device lookup table, a small norm workspace).
+ *     layout (host tables; on the device the block lookup table, a table of
+ *     16384-element runs of each param for the norm, and a small norm
+ *     workspace).
  *   - Calls that take a `stream` (a cudaStream_t; NULL = legacy default
  *     stream) only enqueue work on it and never synchronise.  Asynchronous
  *     device faults surface at the caller's next synchronisation, as in CUDA.
@@ -135,9 +137,11 @@ int fp8z1_shard_range(const fp8z1_layout* layout, int32_t rank, int64_t* b0, int
 int fp8z1_copy_lut(const fp8z1_layout* layout, fp8z1_block* host_dst, int64_t capacity);
 
 /* Read and clear the layout's device status word (synchronous; waits for the
- * copy).  Bit 1 (FP8Z1_DEVSTATUS_BADPTR): a fold/unfold met a param pointer
- * in its device pointer array that was null or not elem_size aligned, and
- * skipped the blocks of that param.  0 means no such event since the last read.
+ * copy).  Bit 1 (FP8Z1_DEVSTATUS_BADPTR): a fold, unfold, fused norm or
+ * fused step met a param pointer in its device pointer array that was null or
+ * not element aligned, and skipped the blocks of that param (the norm also
+ * sets found_inf, so the step is skipped).  0 means no such event since the
+ * last read.
  * Errors: EINVAL, ENODEV, ECUDA. */
 #define FP8Z1_DEVSTATUS_BADPTR 1u
 int fp8z1_device_status(const fp8z1_layout* layout, uint32_t* bits);
