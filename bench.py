@@ -671,8 +671,7 @@ def main():
                     help="keep only the first K experts of each 3-D param (a smaller case)")
     ap.add_argument("--pipeline", type=int, default=-1,
                     help="enqueue each step before the previous one's found_inf is read "
-                         "(launch_step_async); -1: on for the block scheme's fused path, off for MX, "
-                         "whose select kernel runs 2-3%% slower than its plain one")
+                         "(launch_step_async); -1: on for MX and the block scheme's fused path")
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)
@@ -684,7 +683,7 @@ def main():
     ap.add_argument("--ref-sample-experts", type=int, default=1)
     args = ap.parse_args()
     if args.pipeline < 0:
-        args.pipeline = int(args.scheme == "block" and args.path == "fused")
+        args.pipeline = int(args.scheme == "mx" or args.path == "fused")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 

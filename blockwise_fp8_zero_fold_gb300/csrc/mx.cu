@@ -12,10 +12,18 @@
 // block-wise one.  There is no table and no CTA barrier: a group is 8
 // consecutive lanes (one float4 each), its amax three shuffles.
 //
+// Work split: a warp tile is 128 consecutive chunks (2 KB of each FP32
+// array); each CTA takes its own run of 32 consecutive tiles, its 8 warps on
+// consecutive tiles (4 each), 2 CTAs resident per SM.  Runs of 16 to 64
+// tiles were within about 1% of each other on buffers of 88 M to 1.41 G
+// elements; 8 (one tile per warp) lost 8-15% and 512 up to 30%.  A persistent
+// grid-stride loop (8 CTAs per SM over the whole buffer) ran the MoE buffer
+// in 6.08-6.11 ms on some GB300s and 6.45 ms on others; this split ran it in
+// 5.90 ms on one of the latter.
+//
 // fp8z1_mx_step_select runs the same body with a second scalar set picked by
-// a device flag, in its own kernel with its own argument struct: adding
-// fields to MxArgs alone changed the plain kernel's register allocation (65 to
-// 59 registers) and cost it about 4% (6.12 to 6.36 ms on the MoE buffer).
+// a device flag, in its own kernel with its own argument struct (the plain
+// kernel's parameters stay what it reads).
 #include "update.cuh"
 
 namespace {
@@ -45,21 +53,26 @@ struct MxSelArgs {
     StepScalars c2;
 };
 
-// Each warp takes kMxUnroll x 32 consecutive chunks per iteration (for each
-// u, its 32 lanes hold 4 whole groups) and issues every load of them before
-// any update; with 3 CTAs resident per SM (24 warps) that keeps about 96 KB
-// of loads in flight per SM.
-constexpr int kMxUnroll = 2;
+// A warp tile is kMxUnroll x 32 consecutive chunks (for each u, the 32 lanes
+// hold 4 whole groups); the warp issues every load of a tile before any
+// update: with 2 CTAs resident per SM (16 warps) about 128 KB of loads in
+// flight per SM.
+constexpr int kMxUnroll = 4;
+constexpr int kMxTile = 32 * kMxUnroll;  // chunks
+constexpr int64_t kMxTilesPerCta = 32;
 
-// The update and quantise of this warp's chunks, with the scalars c.
+// The update and quantise of this CTA's run of tiles, with the scalars c.
 __device__ __forceinline__ void mx_body(const MxArgs& a, const StepScalars& c, float gs)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t warp = (int64_t)blockIdx.x * (kMxThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kMxThreads / 32);
+    const int64_t ntiles = (a.n_chunks + kMxTile - 1) / kMxTile;
+    const int64_t t0 = (int64_t)blockIdx.x * ntiles / gridDim.x;
+    const int64_t t1 = (int64_t)(blockIdx.x + 1) * ntiles / gridDim.x;
     // the trip count is uniform across a warp, so the group shuffles always see
-    // all 32 lanes; a group's 8 lanes are in or out of range together
-    for (int64_t wbase = warp * (32 * kMxUnroll); wbase < a.n_chunks; wbase += nwarps * (32 * kMxUnroll)) {
+    // all 32 lanes; a group's 8 lanes are in or out of range together (tiles
+    // start at multiples of 8 chunks, and so does the end of the last group)
+    for (int64_t t = t0 + (threadIdx.x >> 5); t < t1; t += kMxThreads / 32) {
+        const int64_t wbase = t * kMxTile;
         float4 g4[kMxUnroll], p4[kMxUnroll], m4[kMxUnroll], v4[kMxUnroll];
 #pragma unroll
         for (int u = 0; u < kMxUnroll; ++u) {
@@ -110,7 +123,7 @@ __device__ __forceinline__ void mx_body(const MxArgs& a, const StepScalars& c, f
 }
 
 // Scalars by value (the plain step).
-__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
+__global__ void __launch_bounds__(kMxThreads, 2) mx_step_kernel(const MxArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
@@ -120,7 +133,7 @@ __global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel(const MxArgs a)
 }
 
 // Two scalar sets by value, picked by *select behind one uniform branch.
-__global__ void __launch_bounds__(kMxThreads, 3) mx_step_kernel_select(const MxSelArgs sa)
+__global__ void __launch_bounds__(kMxThreads, 2) mx_step_kernel_select(const MxSelArgs sa)
 {
     if (*sa.a.found_inf != 0) return;  // skipped step: write nothing
     __shared__ float s_gscale;
@@ -165,10 +178,14 @@ int mx_step_impl(const fp8z1_mx_layout* L, const fp8z1_adamw_hp* hp, const fp8z1
     a.found_inf = d_found_inf;
     a.n_chunks = chunks;
     a.c = scalars(hp);
-    // a persistent grid: 8 CTAs of 256 threads per SM (3 resident), no more than the chunks need
-    int64_t grid = (int64_t)L->sm_count * 8;
-    const int64_t need = (chunks + kMxThreads * kMxUnroll - 1) / (kMxThreads * kMxUnroll);
-    if (grid > need) grid = need;
+    // runs of 32 tiles; a buffer too small to give every SM two such CTAs gets
+    // runs of one tile per warp (or fewer CTAs) instead
+    const int64_t ntiles = (chunks + kMxTile - 1) / kMxTile;
+    int64_t grid = (ntiles + kMxTilesPerCta - 1) / kMxTilesPerCta;
+    if (grid < 2 * (int64_t)L->sm_count) {
+        const int64_t per_warp = (ntiles + kMxThreads / 32 - 1) / (kMxThreads / 32);
+        grid = per_warp < 2 * (int64_t)L->sm_count ? per_warp : 2 * (int64_t)L->sm_count;
+    }
     fp8z1::count_launch();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d_select) {

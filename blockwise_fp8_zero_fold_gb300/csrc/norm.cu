@@ -11,21 +11,27 @@
 // §参数布局变换: the reduced grads are folded into the optimizer's layout.
 //
 // Accuracy: each square is split exactly into float hi + lo parts
-// (x*x and fma(x, x, -x*x)), and a thread adds its 32 squares of a block with
-// error-free two-sums, so its per-block partial is within about 32^2 ulp^2 of
-// the exact value; partials are then summed in double.  The result is well
-// inside 1e-12 relative of the exact sum -- close enough that the clip
-// coefficient formed from it rounds to the same FP32 number as one formed from
-// the exact sum, except in rare ties.  The float path is exact enough only
-// while the partial stays in [2^-90, 2^100), or is 0 because every value is 0:
-// an inf or nan, a square that overflows, or tiny values (whose squares
-// underflow, possibly to a partial of 0) land outside, and then the thread
-// redoes those 32 values in double, where the square of any float is exact.
+// (x*x and fma(x, x, -x*x)), and a thread adds its 32 squares of a unit (half
+// a block, below) with error-free sums -- in two interleaved chains of 16,
+// each step a Fast2Sum of the larger and the smaller of the running sum and
+// the new square (both non-negative), the two chains joined by one more -- so
+// its per-unit partial is within about 32^2 ulp^2 of the exact value;
+// partials are then summed in double.  The result is well inside 1e-12
+// relative of the exact sum -- close enough that the clip coefficient formed
+// from it rounds to the same FP32 number as one formed from the exact sum,
+// except in rare ties.  The float path is exact enough only while the partial
+// stays in [2^-90, 2^100), or is 0 because every value is 0: an inf or nan, a
+// square that overflows, or tiny values (whose squares underflow, possibly to
+// a partial of 0) land outside, and then the thread redoes those 32 values in
+// double, where the square of any float is exact.
 //
-// Latency: a persistent CTA per SM walks a contiguous run of blocks; each
-// thread loads the next block's 32 values (and, reading row-major, looks up
-// the block after that in the table) while it sums the current ones, so a
-// CTA always has a block's worth of loads in flight.
+// Latency: the unit of work is half a block (8192 values; read row-major, 64
+// rows of a block).  Three persistent CTAs of 256 threads per SM each walk a
+// contiguous run of units; each thread loads the next unit's 32 values (and,
+// reading row-major, looks up the block after that in the table) while it sums
+// the current ones, so an SM always has three units' worth of loads in flight.
+// A pure read of this shape reaches about 7.5 TB/s on a GB300; one CTA of 512
+// threads per SM holding whole blocks reached about 6.4.
 //
 // Reduction: each CTA writes one double to a workspace, and the last CTA to
 // finish (an atomic ticket, no waiting) adds the partials in a fixed order.
@@ -39,33 +45,41 @@
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kVec = FP8Z1_BLOCK_ELEMS / 4 / kThreads;  // 8 float4 per thread and block
+constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 3;
+constexpr int kVec = 8;                                           // float4 per thread and unit
+constexpr int kUnitElems = kThreads * kVec * 4;                   // 8192: half a block
+constexpr int kUnitsPerBlock = FP8Z1_BLOCK_ELEMS / kUnitElems;    // 2
+constexpr int kUnitRows = FP8Z1_TILE / kUnitsPerBlock;            // 64 rows of a block
 constexpr int kWarps = kThreads / 32;
+static_assert(kUnitsPerBlock * kUnitElems == FP8Z1_BLOCK_ELEMS, "a block is a whole number of units");
+static_assert(kUnitRows * FP8Z1_TILE == kUnitElems, "a unit is whole rows of a block");
 
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err)
+// a + b = s + err exactly, for a, b >= 0 (Dekker's Fast2Sum on max, min).
+// An inf gives s = inf; a nan is dropped by fmaxf / fminf, so the caller
+// must see it elsewhere (add_square: in lo).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& err)
 {
-    s = __fadd_rn(a, b);
-    const float bb = __fsub_rn(s, a);
-    const float aa = __fsub_rn(s, bb);
-    err = __fadd_rn(__fsub_rn(a, aa), __fsub_rn(b, bb));
+    const float big = fmaxf(a, b), small = fminf(a, b);
+    s = __fadd_rn(big, small);
+    err = __fsub_rn(small, __fsub_rn(s, big));
 }
 
-__device__ __forceinline__ void add_square(float x, float& hi, float& lo, unsigned& nz)
+// hi + lo += x*x.  A nan x makes lo nan (e is nan); an inf x makes hi inf.
+__device__ __forceinline__ void add_square(float x, float& hi, float& lo)
 {
-    nz |= __float_as_uint(x) & 0x7fffffffu;  // any nonzero magnitude
     const float sq = __fmul_rn(x, x);
     const float e = __fmaf_rn(x, x, -sq);  // x*x = sq + e exactly (no under/overflow)
     float t;
-    two_sum(hi, sq, hi, t);
+    fast_two_sum(hi, sq, hi, t);
     lo = __fadd_rn(lo, __fadd_rn(t, e));
 }
 
-// The float partial is exact enough when it lies in [2^-90, 2^100), or when
-// every value was zero (nz == 0).
-__device__ __forceinline__ bool float_path_ok(float hi, unsigned nz)
+// The float partial is exact enough when it lies in [2^-90, 2^100) and lo is
+// a number, or when every value was zero (nz == 0).
+__device__ __forceinline__ bool float_path_ok(float hi, float lo, unsigned nz)
 {
-    return hi < 0x1p100f && (hi >= 0x1p-90f || nz == 0u);
+    return hi < 0x1p100f && lo == lo && (hi >= 0x1p-90f || nz == 0u);
 }
 
 __device__ __forceinline__ void add_square_exact(float x, double& acc, int& bad)
@@ -83,18 +97,24 @@ __device__ __forceinline__ double warp_sum(double v)
     return v;
 }
 
-__device__ __forceinline__ void sum_block(const float4 (&x)[kVec], double& acc, int& bad)
+__device__ __forceinline__ void sum_unit(const float4 (&x)[kVec], double& acc, int& bad)
 {
-    float hi = 0.0f, lo = 0.0f;
-    unsigned nz = 0u;
+    float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
+    unsigned bits = 0u;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-        add_square(x[j].x, hi, lo, nz);
-        add_square(x[j].y, hi, lo, nz);
-        add_square(x[j].z, hi, lo, nz);
-        add_square(x[j].w, hi, lo, nz);
+        bits |= __float_as_uint(x[j].x) | __float_as_uint(x[j].y) | __float_as_uint(x[j].z) |
+                __float_as_uint(x[j].w);
+        add_square(x[j].x, hi0, lo0);
+        add_square(x[j].y, hi1, lo1);
+        add_square(x[j].z, hi0, lo0);
+        add_square(x[j].w, hi1, lo1);
     }
-    if (float_path_ok(hi, nz)) {
+    float hi, t;
+    fast_two_sum(hi0, hi1, hi, t);
+    const float lo = __fadd_rn(__fadd_rn(lo0, lo1), t);
+    const unsigned nz = bits & 0x7fffffffu;  // any nonzero magnitude
+    if (float_path_ok(hi, lo, nz)) {
         acc += (double)hi;
         acc += (double)lo;
     } else {
@@ -108,13 +128,15 @@ __device__ __forceinline__ void sum_block(const float4 (&x)[kVec], double& acc, 
     }
 }
 
-// Where the grads of one unit of work come from: the folded shard, a block of
-// the row-major params (through the block table), a run of at most 16384
+// Where the grads of one block come from: the folded shard, a block of the
+// row-major params (through the block table), a run of at most 16384
 // consecutive elements of a param the range holds whole (from the layout's
 // run table), or a run of at most 16384 elements of one contiguous span of a
 // param (whole row-block strips of a param the range cuts: a strip is 128
 // full rows, and consecutive strips are consecutive in memory).  A sum of
 // squares needs no block structure, so only partial strips need the table.
+// Each of these is two units: its first and second 8192 values (for a block
+// of the row-major params, its rows 0-63 and 64-127).
 enum Src { kFolded, kRows, kParams, kSpan };
 
 // Where unit k's grads live in the row-major params.
@@ -178,8 +200,8 @@ struct NormArgs {
     int64_t span_elems;           // ... its length ...
     int32_t span_param;           // ... and the param
     float4* store;                // STORE: folded grads at block b0
-    int64_t b0;                   // first block (kRows: LUT index) or unit (kParams)
-    int64_t nblocks;              // blocks of 16384, the last one possibly partial
+    int64_t b0;                   // first block (kRows: LUT index) or run (kParams)
+    int64_t nblocks;              // blocks of 16384, the last one possibly partial (2 units each)
     int64_t tail_k;               // kFolded: index of a partial last block ...
     int tail_vec4;                // ... and its float4 count (0: no partial block)
     double* partials;             // one per CTA
@@ -189,35 +211,36 @@ struct NormArgs {
     int32_t* found_inf;
 };
 
-// Issue the loads of unit k (index from b0): this thread's 32 values.  For a
-// block, chunk j is tid + 512 j: block row (tid + 512 j) / 32, columns
-// 4 * ((tid + 512 j) % 32) .. + 3; for a run of a param, elements
-// 4 (tid + 512 j) .. + 3.  Zeros outside the real extent.
+// Issue the loads of unit u (index from the launch's first block; the block
+// is u / 2, h = u % 2 its half): this thread's 32 values.  Chunk j is
+// ci = tid + 256 j of the unit: for a block, block row 64 h + ci / 32 and
+// columns 4 (ci % 32) .. + 3; for a run of a param, elements
+// 8192 h + 4 ci .. + 3.  Zeros outside the real extent.
 template <Src SRC>
-__device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
-                                           float4 (&x)[kVec])
+__device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, int64_t u, int tid,
+                                          float4 (&x)[kVec])
 {
+    const int h = (int)(u % kUnitsPerBlock);
     if constexpr (SRC == kFolded) {
-        const float4* p = a.g + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
-        if (a.tail_vec4 != 0 && k == a.tail_k) {  // a flat range's partial last block
+        // float4s of this unit that exist: all of them, except in a flat
+        // range's partial last block
+        int lim = kUnitElems / 4;
+        if (a.tail_vec4 != 0 && u / kUnitsPerBlock == a.tail_k) lim = a.tail_vec4 - h * (kUnitElems / 4);
+        const float4* p = a.g + u * (kUnitElems / 4) + tid;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                x[j] = tid + j * kThreads < a.tail_vec4 ? __ldcs(p + j * kThreads)
-                                                        : make_float4(0.f, 0.f, 0.f, 0.f);
-            return;
-        }
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+        for (int j = 0; j < kVec; ++j)
+            x[j] = tid + j * kThreads < lim ? __ldcs(p + j * kThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
     } else if constexpr (SRC == kParams || SRC == kSpan) {
+        const int e0 = h * kUnitElems;
         if (s.vec && s.count == FP8Z1_BLOCK_ELEMS) {  // a whole, aligned run
-            const float4* p = reinterpret_cast<const float4*>(s.tile) + tid;
+            const float4* p = reinterpret_cast<const float4*>(s.tile + e0) + tid;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
             return;
         }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            const int e = 4 * (tid + j * kThreads);
+            const int e = e0 + 4 * (tid + j * kThreads);
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (!s.bad && e < s.count) {
                 const float* src = s.tile + e;
@@ -233,10 +256,11 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
             x[j] = v;
         }
     } else {
+        const int r0 = h * kUnitRows;
         if (s.vec && s.rows == FP8Z1_TILE && s.cols == FP8Z1_TILE) {
-            // a full, aligned block: chunk j sits 16 rows below chunk j-1
-            const float* src = s.tile + (int64_t)(tid >> 5) * s.ld + ((tid & 31) << 2);
-            const int64_t step = 16 * s.ld;
+            // a full, aligned block: chunk j sits 8 rows below chunk j-1
+            const float* src = s.tile + (int64_t)(r0 + (tid >> 5)) * s.ld + ((tid & 31) << 2);
+            const int64_t step = (kThreads / 32) * s.ld;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) x[j] = __ldcs(reinterpret_cast<const float4*>(src + j * step));
             return;
@@ -244,7 +268,7 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             const int ci = tid + j * kThreads;
-            const int r = ci >> 5, c = (ci & 31) << 2;
+            const int r = r0 + (ci >> 5), c = (ci & 31) << 2;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (!s.bad && r < s.rows) {
                 const float* src = s.tile + r * s.ld + c;
@@ -262,19 +286,23 @@ __device__ __forceinline__ void load_block(const NormArgs& a, const RowSrc& s, i
     }
 }
 
+// Where unit u's block lives.
 template <Src SRC>
-__device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t k)
+__device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t u)
 {
+    const int64_t k = u / kUnitsPerBlock;
     if (SRC == kRows) return row_src(a.lut, a.params, a.b0 + k);
     if (SRC == kParams) return param_src(a.units, a.params, a.b0 + k);
     if (SRC == kSpan) return span_src(a.params, a.span_param, a.span_offset, a.span_elems, k);
     return RowSrc{};
 }
 
-// Sum (and store) unit k, whose values are in x.
+// Sum (and store) unit u, whose values are in x.  Folded, unit u is the
+// 8192 consecutive values from 8192 u: chunk ci of it holds elements
+// 4 ci .. + 3, which is where load_unit took them from.
 template <Src SRC, bool STORE>
-__device__ __forceinline__ void finish_block(const NormArgs& a, const RowSrc& s, int64_t k, int tid,
-                                             const float4 (&x)[kVec], double& acc, int& bad)
+__device__ __forceinline__ void finish_unit(const NormArgs& a, const RowSrc& s, int64_t u, int tid,
+                                            const float4 (&x)[kVec], double& acc, int& bad)
 {
     if (SRC != kFolded && s.bad) {  // unreadable grads: nothing is summed or stored
         if (tid == 0) atomicOr(a.status, FP8Z1_DEV_BADPTR);
@@ -282,46 +310,47 @@ __device__ __forceinline__ void finish_block(const NormArgs& a, const RowSrc& s,
         return;
     }
     if (STORE) {
-        float4* dst = a.store + k * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+        float4* dst = a.store + u * (kUnitElems / 4) + tid;
 #pragma unroll
         for (int j = 0; j < kVec; ++j) __stcs(dst + j * kThreads, x[j]);
     }
-    sum_block(x, acc, bad);
+    sum_unit(x, acc, bad);
 }
 
 template <Src SRC, bool STORE>
-__global__ void __launch_bounds__(kThreads, 1) norm_kernel(const NormArgs a)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) norm_kernel(const NormArgs a)
 {
     __shared__ double s_part[kWarps];
     __shared__ int s_last;
     const int tid = threadIdx.x;
-    const int64_t k0 = (int64_t)blockIdx.x * a.nblocks / gridDim.x;
-    const int64_t k1 = (int64_t)(blockIdx.x + 1) * a.nblocks / gridDim.x;
+    const int64_t nunits = a.nblocks * kUnitsPerBlock;
+    const int64_t u0 = (int64_t)blockIdx.x * nunits / gridDim.x;
+    const int64_t u1 = (int64_t)(blockIdx.x + 1) * nunits / gridDim.x;
 
     double acc = 0.0;
     int bad = 0;
-    // Two register buffers.  Loop invariant at the head: xa holds block k
-    // (loads issued), sa = where block k lives, sb = where block k+1 lives.
+    // Two register buffers.  Loop invariant at the head: xa holds unit u
+    // (loads issued), sa = where unit u lives, sb = where unit u+1 lives.
     float4 xa[kVec], xb[kVec];
     RowSrc sa = {}, sb = {};
-    int64_t k = k0;
-    if (k < k1) {
-        sa = src_of<SRC>(a, k);
-        load_block<SRC>(a, sa, k, tid, xa);
-        if (k + 1 < k1) sb = src_of<SRC>(a, k + 1);
+    int64_t u = u0;
+    if (u < u1) {
+        sa = src_of<SRC>(a, u);
+        load_unit<SRC>(a, sa, u, tid, xa);
+        if (u + 1 < u1) sb = src_of<SRC>(a, u + 1);
     }
-    while (k < k1) {
-        if (k + 1 < k1) load_block<SRC>(a, sb, k + 1, tid, xb);
+    while (u < u1) {
+        if (u + 1 < u1) load_unit<SRC>(a, sb, u + 1, tid, xb);
         RowSrc sc = {};
-        if (k + 2 < k1) sc = src_of<SRC>(a, k + 2);
-        finish_block<SRC, STORE>(a, sa, k, tid, xa, acc, bad);
-        if (++k >= k1) break;
-        // xb holds block k, sb = where it lives, sc = where block k+1 lives
-        if (k + 1 < k1) load_block<SRC>(a, sc, k + 1, tid, xa);
+        if (u + 2 < u1) sc = src_of<SRC>(a, u + 2);
+        finish_unit<SRC, STORE>(a, sa, u, tid, xa, acc, bad);
+        if (++u >= u1) break;
+        // xb holds unit u, sb = where it lives, sc = where unit u+1 lives
+        if (u + 1 < u1) load_unit<SRC>(a, sc, u + 1, tid, xa);
         RowSrc sd = {};
-        if (k + 2 < k1) sd = src_of<SRC>(a, k + 2);
-        finish_block<SRC, STORE>(a, sb, k, tid, xb, acc, bad);
-        ++k;
+        if (u + 2 < u1) sd = src_of<SRC>(a, u + 2);
+        finish_unit<SRC, STORE>(a, sb, u, tid, xb, acc, bad);
+        ++u;
         sa = sc;
         sb = sd;
     }
@@ -358,11 +387,13 @@ __global__ void __launch_bounds__(kThreads, 1) norm_kernel(const NormArgs a)
     }
 }
 
-// one CTA of 512 threads per SM, at most one per block and one per partial slot
-int64_t persistent_grid(const fp8z1_layout* L, int64_t n)
+// three CTAs of 256 threads per SM, at most one per unit (n blocks: 2n units)
+// and one per partial slot
+template <typename Layout>
+int64_t persistent_grid(const Layout* L, int64_t n)
 {
-    int64_t grid = (int64_t)L->sm_count;
-    if (grid > n) grid = n;
+    int64_t grid = (int64_t)L->sm_count * kCtasPerSm;
+    if (grid > n * kUnitsPerBlock) grid = n * kUnitsPerBlock;
     if (grid > L->max_partials) grid = L->max_partials;
     return grid;
 }
@@ -507,11 +538,9 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
     a.counter = L->d_counter;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
-    int64_t grid = L->sm_count;
-    if (grid > a.nblocks) grid = a.nblocks;
-    if (grid > L->max_partials) grid = L->max_partials;
     fp8z1::count_launch();
-    norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    norm_kernel<kFolded, false><<<(unsigned)persistent_grid(L, a.nblocks), kThreads, 0,
+                                 static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
 

@@ -83,10 +83,14 @@ def test_ranges_accumulate_to_full_and_are_deterministic(layout):
     assert abs(s2.item() - want) > 1e-3 * want
 
 
-@pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan")])
-@pytest.mark.parametrize("where", [0, 5 * 16384 + 77, NBLK * 16384 - 1])
-def test_found_inf(layout, bad, where):
-    g = np.ones(NBLK * 16384, np.float32)
+@pytest.mark.parametrize("fill", [1.0, 0.0])
+@pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan"), -float("nan")])
+@pytest.mark.parametrize("where", [0, 5 * 16384 + 77, 5 * 16384 + 8192 + 2, NBLK * 16384 - 1])
+def test_found_inf(layout, bad, where, fill):
+    # A nan leaves the running float sum of squares finite (max / min drop it)
+    # and shows only in its low part; next to zeros the sum stays 0.  Both must
+    # still send the unit to the double path, which raises the flag.
+    g = np.full(NBLK * 16384, fill, np.float32)
     g[where] = bad
     dg = torch.from_numpy(g).cuda()
     _, found, _, _ = _norm(layout, dg, 0, NBLK)
