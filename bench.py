@@ -134,6 +134,22 @@ def _workload(args, synth):
     return w if shapes == w.shapes else synth.workload(args.workload, dp=1, rank=0, shapes=shapes)
 
 
+def _time_layout_build(F, shapes, dp, reps=3):
+    """Host wall time of the one-time layout build (block table, run table,
+    shard ranges) and of the build plus its upload to the device; medians."""
+    host, full = [], []
+    for _ in range(reps):
+        t = time.perf_counter()
+        L = F.fp8z1_build_layout(shapes, dp_size=dp, host_only=True)
+        host.append((time.perf_counter() - t) * 1e3)
+        del L
+        t = time.perf_counter()
+        L = F.fp8z1_build_layout(shapes, dp_size=dp)
+        full.append((time.perf_counter() - t) * 1e3)
+        del L
+    return {"host": statistics.median(host), "host_and_upload": statistics.median(full)}
+
+
 def _workload_label(args, shapes) -> str:
     cut = "".join([f"[{args.experts} experts]" if args.experts else "",
                    f"[first {args.params} params]" if args.params else ""])
@@ -173,6 +189,7 @@ def bench_ours(args, rank, world, dist):
     grads = synth.make_grads(w, 1, dev)
     fp8 = [torch.zeros(s, dtype=torch.uint8, device=dev) for s in w.shapes]
     torch.cuda.synchronize()
+    layout_ms = _time_layout_build(F, w.shapes, dp)
     stream = torch.cuda.current_stream()
     # the shard's blocks, padded elements and real elements (whole buffer: all)
     nblk = opt.b1 - opt.b0
@@ -400,6 +417,7 @@ def bench_ours(args, rank, world, dist):
         "skipped_steps": skipped,
         "e2e": e2e,
         "bf16_fold": bf16,
+        "layout_build_ms": layout_ms,
     }
     if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)

@@ -60,6 +60,8 @@ def test_bench_line_tiny():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["other_path"]["path"] == "unfused"
+    lb = d["layout_build_ms"]
+    assert 0 < lb["host"] and 0 < lb["host_and_upload"]
     # per step: the flat-run norm, and the step (one launch; two gated ones for a
     # padded run when the step picks its scalars by the previous step's flag)
     assert 2 * 4 <= d["gpu_launches"] <= 3 * 4

@@ -195,6 +195,45 @@ def test_mx_moe_full_size_sampled(lib):
             assert np.array_equal(to_host(buf.view(-1, 32)[idx]).view(np.uint32), st.view(np.uint32))
 
 
+# Each MX launch cuts its warp tiles (128 float4 chunks) into one run per CTA:
+# runs of 32 tiles on a large buffer, fewer CTAs of smaller runs on a small
+# one.  Every element of these buffers is checked, so every run boundary is:
+# (3, 1000, 2016) is 11 813 tiles (the last one partial) in 370 runs of ~32;
+# (1, 700, 3008) is 4 113 tiles over 304 CTAs of ~13.5; (1, 40, 3008) is 235
+# tiles, one per warp.  Rank 1 of 2 starts the shard mid-buffer.
+@pytest.mark.parametrize("shape", [(3, 1000, 2016), (1, 700, 3008), (1, 40, 3008)])
+@pytest.mark.parametrize("dp,rank", [(1, 0), (2, 1)])
+def test_mx_step_every_element(lib, shape, dp, rank):
+    rng = np.random.default_rng(shape[1] + 10 * rank)
+    L = F.fp8z1_mx_build_layout([shape], dp_size=dp)
+    groups, n = F.fp8z1_mx_layout_info(L)
+    g0, g1 = F.fp8z1_mx_shard_range(L, rank)
+    sl = slice(g0 * 32, g1 * 32)
+    ps = (rng.standard_normal(n) * 0.02).astype(np.float32)[sl].copy()
+    ms = (rng.standard_normal(n) * 1e-4).astype(np.float32)[sl].copy()
+    vs = np.abs(rng.standard_normal(n) * 1e-8).astype(np.float32)[sl].copy()
+    dpp, dm, dv = (torch.from_numpy(x.copy()).cuda() for x in (ps, ms, vs))
+    dq = torch.full(((g1 - g0) * 32,), 0x7F, dtype=torch.uint8, device="cuda")
+    ds = torch.full((g1 - g0,), 0xFF, dtype=torch.uint8, device="cuda")
+    for t in (1, 2):
+        gh = (rng.standard_normal(n) * 1024e-4).astype(np.float32)
+        dg = torch.from_numpy(gh).cuda()
+        s = torch.zeros(1, dtype=torch.float64, device="cuda")
+        f = torch.zeros(1, dtype=torch.int32, device="cuda")
+        F.fp8z1_mx_grad_norm(L, dg, 0, groups, s, f)
+        hp = _hp(step=t)
+        F.fp8z1_mx_step(L, F.make_hp(**hp), dg[g0 * 32:], dpp, dm, dv, dq, ds, g0, g1, s, f)
+        torch.cuda.synchronize()
+        os_, of = oracle.sumsq(gh)
+        assert of == 0 and abs(s.item() - os_) <= 1e-12 * os_
+        q, sc, skipped = oracle.mx_step(oracle.make_hp(**hp), os_, of, gh[sl].copy(), ps, ms, vs)
+        assert not skipped
+        for a, b, what in [(dpp, ps, "master"), (dm, ms, "m"), (dv, vs, "v")]:
+            assert np.array_equal(to_host(a).view(np.uint32), b.view(np.uint32)), what
+        assert np.array_equal(to_host(dq), q)
+        assert np.array_equal(to_host(ds), sc)
+
+
 def test_mx_optimizer_steps_and_scaler(lib):
     """MxShardOptimizer over four steps, the third with an inf (skipped: S
     halves, t stays; growth every 2 clean steps), against the oracle's MX
