@@ -105,6 +105,27 @@ def test_bad_param_pointer_is_reported_not_touched(lib):
     assert np.array_equal(got[16384:], oracle.fold(shapes, hp, 1, 3))
 
 
+@pytest.mark.parametrize("esz", [1, 2])
+def test_bad_param_pointer_mid_run_unfold(lib, esz):
+    """The narrow unfolds copy runs of several blocks per CTA: a null param in
+    the middle of a run (blocks 1-2 of 0-4) is skipped and reported, and the
+    run carries on with the blocks after it."""
+    shapes = [(1, 128, 128), (1, 256, 128), (1, 128, 256)]
+    hp = _host_params(shapes, esz, seed=8)
+    L = F.fp8z1_build_layout(shapes)
+    nblk = F.fp8z1_layout_info(L)[0]
+    assert nblk == 5
+    buf = _dev(oracle.fold(shapes, hp).view(NP_OF[esz]))
+    outs = [torch.full(s, _SENTINEL[esz], dtype=TORCH_OF[esz], device="cuda") for s in shapes]
+    ptrs = torch.tensor([outs[0].data_ptr(), 0, outs[2].data_ptr()], dtype=torch.int64, device="cuda")
+    F.fp8z1_unfold(L, buf, ptrs, esz, 0, nblk)
+    torch.cuda.synchronize()
+    assert F.fp8z1_device_status(L) == F.DEVSTATUS_BADPTR
+    assert np.array_equal(bytes_of(outs[0]), bytes_of(hp[0]))
+    assert np.array_equal(bytes_of(outs[2]), bytes_of(hp[2]))
+    assert (bytes_of(outs[1]) == 0x3C).all()  # the sentinel's bytes: untouched
+
+
 def test_alignment_and_range_errors(lib):
     L = F.fp8z1_build_layout([(1, 300, 200)])
     p = torch.zeros(6 * 16384 + 4, dtype=torch.float32, device="cuda")
