@@ -120,10 +120,14 @@ __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScala
         }
         const int64_t i = base + j * kThreads;
         float4 g4;
-        if (GRAD_ROWS)
-            g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec);
-        else
+        if (GRAD_ROWS) {
+            if (!PAD && gvec)  // a full tile (every launch without PAD), 16-byte rows
+                g4 = __ldcs(reinterpret_cast<const float4*>(gtile + (int64_t)(row0 + 16 * j) * ld + col));
+            else
+                g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec);
+        } else {
             g4 = __ldcs(a.grad + i);
+        }
         float4 p4 = a.master[i];
         float4 m4 = a.mom1[i];
         float4 v4 = a.mom2[i];
@@ -233,7 +237,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
         if (CODES_ROWS) {
             const int ci = tid + j * kThreads;
-            store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
+            if (!PAD && cvec)  // a full tile, 4-byte aligned rows
+                __stcs(reinterpret_cast<unsigned int*>(ctile + (int64_t)(ci >> 5) * ld + ((ci & 31) << 2)), q);
+            else
+                store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
         }
         if (MON) {
             const float2 d01 = e4m3x2_decode(lo), d23 = e4m3x2_decode(hi);
