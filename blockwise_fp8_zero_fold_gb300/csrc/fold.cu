@@ -16,7 +16,7 @@
 // block side (contiguous) and on the row-major side (a row segment is 128 *
 // elem_size contiguous bytes).  Otherwise each thread moves single elements,
 // still coalesced along rows.
-#include "internal.h"
+#include "checked.cuh"
 
 namespace {
 
@@ -38,8 +38,9 @@ __device__ __forceinline__ void st_stream16(uint8_t* p, uint4 v)
 }
 
 // Copy one block between its row-major tile and its place buf in the shard.
+// elems: the param's extent, against which a checked build tests each access.
 template <int ESZ, bool FOLD>
-__device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base, uint8_t* buf)
+__device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base, uint8_t* buf, int64_t elems)
 {
     using T = typename ElemT<ESZ>::T;
     uint8_t* const tile = base + blk.src_offset * ESZ;
@@ -60,7 +61,10 @@ __device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base
                 const int r = i / kVPR, c = i % kVPR;
                 const bool real = r < rows && c < cv;
                 if (FOLD)
-                    v[u] = real ? ld_stream16(tile + r * ld + c * 16) : make_uint4(0, 0, 0, 0);
+                    v[u] = real && fp8z1::in_extent(blk.src_offset + (int64_t)r * blk.ld + c * (16 / ESZ), 16 / ESZ,
+                                                    elems)
+                               ? ld_stream16(tile + r * ld + c * 16)
+                               : make_uint4(0, 0, 0, 0);
                 else if (real)
                     v[u] = ld_stream16(buf + (int64_t)i * 16);
             }
@@ -70,7 +74,8 @@ __device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base
                 const int r = i / kVPR, c = i % kVPR;
                 if (FOLD)
                     st_stream16(buf + (int64_t)i * 16, v[u]);
-                else if (r < rows && c < cv)
+                else if (r < rows && c < cv &&
+                         fp8z1::in_extent(blk.src_offset + (int64_t)r * blk.ld + c * (16 / ESZ), 16 / ESZ, elems))
                     st_stream16(tile + r * ld + c * 16, v[u]);
             }
         }
@@ -86,7 +91,9 @@ __device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base
                 const int r = i / FP8Z1_TILE, c = i % FP8Z1_TILE;
                 const bool real = r < rows && c < cols;
                 if (FOLD)
-                    v[u] = real ? reinterpret_cast<const T*>(tile + r * ld)[c] : T(0);
+                    v[u] = real && fp8z1::in_extent(blk.src_offset + (int64_t)r * blk.ld + c, 1, elems)
+                               ? reinterpret_cast<const T*>(tile + r * ld)[c]
+                               : T(0);
                 else if (real)
                     v[u] = reinterpret_cast<const T*>(buf)[i];
             }
@@ -96,7 +103,7 @@ __device__ __forceinline__ void copy_block(const fp8z1_block& blk, uint8_t* base
                 const int r = i / FP8Z1_TILE, c = i % FP8Z1_TILE;
                 if (FOLD)
                     reinterpret_cast<T*>(buf)[i] = v[u];
-                else if (r < rows && c < cols)
+                else if (r < rows && c < cols && fp8z1::in_extent(blk.src_offset + (int64_t)r * blk.ld + c, 1, elems))
                     reinterpret_cast<T*>(tile + r * ld)[c] = v[u];
             }
         }
@@ -111,7 +118,8 @@ template <int ESZ, bool FOLD, int BPC>
 __global__ void __launch_bounds__(kThreads, (FOLD || ESZ == 1) ? 3 : 2) fold_kernel(const fp8z1_block* __restrict__ lut,
                                                         void* const* __restrict__ params,
                                                         uint8_t* __restrict__ shard, int64_t b0, int64_t n,
-                                                        unsigned* __restrict__ status)
+                                                        unsigned* __restrict__ status,
+                                                        const int64_t* __restrict__ param_elems)
 {
     const int64_t k0 = (int64_t)blockIdx.x * BPC;
     const int64_t k1 = k0 + BPC < n ? k0 + BPC : n;
@@ -127,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, (FOLD || ESZ == 1) ? 3 : 2) fold_ker
         if (base == nullptr || (reinterpret_cast<uintptr_t>(base) % ESZ) != 0) {
             if (threadIdx.x == 0) atomicOr(status, FP8Z1_DEV_BADPTR);
         } else {
-            copy_block<ESZ, FOLD>(blk, base, shard + k * (FP8Z1_BLOCK_ELEMS * ESZ));
+            const int64_t elems = FP8Z1_CHECKED ? param_elems[blk.param] : 0;
+            copy_block<ESZ, FOLD>(blk, base, shard + k * (FP8Z1_BLOCK_ELEMS * ESZ), elems);
         }
         blk = next;
         base = next_base;
@@ -144,7 +153,8 @@ void launch_esz(const fp8z1_layout* L, void* const* params, uint8_t* shard, int6
                 cudaStream_t stream)
 {
     const dim3 grid((unsigned)((n + BPC - 1) / BPC)), block(kThreads);
-    fold_kernel<ESZ, FOLD, BPC><<<grid, block, 0, stream>>>(L->d_lut, params, shard, b0, n, L->d_status);
+    fold_kernel<ESZ, FOLD, BPC><<<grid, block, 0, stream>>>(L->d_lut, params, shard, b0, n, L->d_status,
+                                                          L->d_param_elems);
 }
 
 template <bool FOLD>
@@ -194,3 +204,5 @@ extern "C" int fp8z1_unfold(const fp8z1_layout* L, const void* src_shard, void* 
     return launch<false>(L, d_dst_params, const_cast<uint8_t*>(static_cast<const uint8_t*>(src_shard)),
                          elem_size, b0, b1, static_cast<cudaStream_t>(stream));
 }
+
+FP8Z1_CHECKED_MISSES_READER(checked_misses_fold)

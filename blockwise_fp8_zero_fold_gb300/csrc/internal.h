@@ -14,6 +14,13 @@
 // that meets device data it cannot use (it then skips that work).
 #define FP8Z1_DEV_BADPTR 1u  // a param pointer was null or not elem_size aligned
 
+// Checked builds (libfp8z1_checked.so, compiled with -DFP8Z1_CHECKED=1) test
+// every access a kernel makes to a row-major param against that param's
+// extent, skip an access that falls outside and count it (checked.cuh).
+#ifndef FP8Z1_CHECKED
+#define FP8Z1_CHECKED 0
+#endif
+
 // A run of at most FP8Z1_BLOCK_ELEMS consecutive row-major elements of one
 // param: what the norm reads for a param that a block range holds whole.
 struct fp8z1_unit {
@@ -41,6 +48,7 @@ struct fp8z1_layout {
     std::vector<int64_t> param_unit0;   // first unit of each param; n_params + 1 entries
     std::vector<fp8z1_unit> units;      // every param cut into units, in param order
     fp8z1_unit* d_units = nullptr;      // device copy of `units`
+    int64_t* d_param_elems = nullptr;   // E * R * C of each param (what checked builds test against)
     // [first, last) block pairs, ascending: runs of at least kFullRunMin blocks
     // whose params have R and C multiples of 128 (every block a full tile)
     std::vector<int64_t> full_runs;
@@ -97,6 +105,15 @@ struct NormPiece {
     int32_t param;  // kSpan
 };
 void norm_pieces(const fp8z1_layout* L, int64_t b0, int64_t b1, std::vector<NormPiece>& out);
+
+#if FP8Z1_CHECKED
+// Out-of-extent accesses each checked translation unit has counted (and
+// skipped) on the current device, since the library was loaded.
+uint64_t checked_misses_fold();
+uint64_t checked_misses_norm();
+uint64_t checked_misses_step_full();
+uint64_t checked_misses_step_pad();
+#endif
 
 // Kernels this library has enqueued in this process (every device and stream),
 // read through fp8z1_kernel_launches.

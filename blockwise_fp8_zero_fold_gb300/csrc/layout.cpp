@@ -24,11 +24,13 @@ void release_device(fp8z1_layout* L)
 {
     cudaFree(L->d_lut);
     cudaFree(L->d_units);
+    cudaFree(L->d_param_elems);
     cudaFree(L->d_partials);
     cudaFree(L->d_counter);
     cudaFree(L->d_status);
     L->d_lut = nullptr;
     L->d_units = nullptr;
+    L->d_param_elems = nullptr;
     L->d_partials = nullptr;
     L->d_counter = nullptr;
     L->d_status = nullptr;
@@ -43,8 +45,17 @@ int upload(fp8z1_layout* L)
     L->max_partials = L->sm_count * 4 < 4096 ? L->sm_count * 4 : 4096;
     const size_t lut_bytes = sizeof(fp8z1_block) * (size_t)L->n_blocks;
     const size_t unit_bytes = sizeof(fp8z1_unit) * L->units.size();
+    std::vector<int64_t> elems;
+    try {
+        elems.resize(L->shapes.size());
+    } catch (...) {
+        return FP8Z1_ENOMEM;
+    }
+    for (size_t i = 0; i < L->shapes.size(); ++i) elems[i] = L->shapes[i].E * L->shapes[i].R * L->shapes[i].C;
+    const size_t elems_bytes = sizeof(int64_t) * elems.size();
     if (cudaMalloc(&L->d_lut, lut_bytes ? lut_bytes : sizeof(fp8z1_block)) != cudaSuccess ||
         cudaMalloc(&L->d_units, unit_bytes ? unit_bytes : sizeof(fp8z1_unit)) != cudaSuccess ||
+        cudaMalloc(&L->d_param_elems, elems_bytes ? elems_bytes : sizeof(int64_t)) != cudaSuccess ||
         cudaMalloc(&L->d_partials, sizeof(double) * (size_t)L->max_partials) != cudaSuccess ||
         cudaMalloc(&L->d_counter, sizeof(unsigned)) != cudaSuccess ||
         cudaMalloc(&L->d_status, sizeof(unsigned)) != cudaSuccess) {
@@ -54,6 +65,8 @@ int upload(fp8z1_layout* L)
     if (lut_bytes && cudaMemcpy(L->d_lut, L->lut.data(), lut_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
         return FP8Z1_ECUDA;
     if (unit_bytes && cudaMemcpy(L->d_units, L->units.data(), unit_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
+        return FP8Z1_ECUDA;
+    if (elems_bytes && cudaMemcpy(L->d_param_elems, elems.data(), elems_bytes, cudaMemcpyHostToDevice) != cudaSuccess)
         return FP8Z1_ECUDA;
     if (cudaMemset(L->d_counter, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(L->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
@@ -216,6 +229,44 @@ extern "C" int fp8z1_kernel_launches(uint64_t* out)
     if (!out) return FP8Z1_EINVAL;
     *out = fp8z1::launch_counter().load(std::memory_order_relaxed);
     return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_build_flags(void)
+{
+    return FP8Z1_CHECKED ? FP8Z1_BUILD_CHECKED : 0;
+}
+
+extern "C" int fp8z1_checked_misses(uint64_t* count)
+{
+    if (!count) return FP8Z1_EINVAL;
+    *count = 0;
+#if FP8Z1_CHECKED
+    const uint64_t parts[] = {fp8z1::checked_misses_fold(), fp8z1::checked_misses_norm(),
+                              fp8z1::checked_misses_step_full(), fp8z1::checked_misses_step_pad()};
+    for (uint64_t v : parts) {
+        if (v == ~0ull) return FP8Z1_ECUDA;
+        *count += v;
+    }
+#endif
+    return FP8Z1_OK;
+}
+
+extern "C" int fp8z1_checked_set_lut_entry(fp8z1_layout* L, int64_t block, const fp8z1_block* entry)
+{
+#if FP8Z1_CHECKED
+    if (!L || !entry || block < 0 || block >= L->n_blocks) return FP8Z1_EINVAL;
+    if (!L->on_device) return FP8Z1_ENODEV;
+    if (cudaMemcpy(L->d_lut + block, entry, sizeof(fp8z1_block), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8Z1_ECUDA;
+    }
+    return FP8Z1_OK;
+#else
+    (void)L;
+    (void)block;
+    (void)entry;
+    return FP8Z1_EINVAL;
+#endif
 }
 
 extern "C" int fp8z1_destroy_layout(fp8z1_layout* L)

@@ -41,7 +41,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "internal.h"
+#include "checked.cuh"
 
 namespace {
 
@@ -147,14 +147,38 @@ struct RowSrc {
     int count;  // kParams, kSpan: elements in the run
     bool vec;   // 16-byte loads (kRows: ld % 4 == 0 and an aligned tile; kParams, kSpan: an aligned run)
     bool bad;   // null or misaligned param pointer
+#if FP8Z1_CHECKED
+    int64_t first;  // element index of tile[0] in its param
+    int64_t elems;  // the param's extent
+#endif
 };
 
+// Whether tile[idx .. idx + w) lies inside its param (checked builds test it).
+__device__ __forceinline__ bool src_ok(const RowSrc& s, int64_t idx, int w)
+{
+#if FP8Z1_CHECKED
+    return fp8z1::in_extent(s.first + idx, w, s.elems);
+#else
+    (void)s;
+    (void)idx;
+    (void)w;
+    return true;
+#endif
+}
+
 __device__ __forceinline__ RowSrc row_src(const fp8z1_block* __restrict__ lut,
-                                          const float* const* __restrict__ params, int64_t k)
+                                          const float* const* __restrict__ params,
+                                          const int64_t* __restrict__ param_elems, int64_t k)
 {
     const fp8z1_block blk = lut[k];
     const float* base = params[blk.param];
     RowSrc s;
+#if FP8Z1_CHECKED
+    s.first = blk.src_offset;
+    s.elems = param_elems[blk.param];
+#else
+    (void)param_elems;
+#endif
     s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
     s.tile = s.bad ? nullptr : base + blk.src_offset;
     s.ld = blk.ld;
@@ -165,11 +189,18 @@ __device__ __forceinline__ RowSrc row_src(const fp8z1_block* __restrict__ lut,
 }
 
 __device__ __forceinline__ RowSrc param_src(const fp8z1_unit* __restrict__ units,
-                                            const float* const* __restrict__ params, int64_t u)
+                                            const float* const* __restrict__ params,
+                                            const int64_t* __restrict__ param_elems, int64_t u)
 {
     const fp8z1_unit un = units[u];
     const float* base = params[un.param];
     RowSrc s = {};
+#if FP8Z1_CHECKED
+    s.first = un.offset;
+    s.elems = param_elems[un.param];
+#else
+    (void)param_elems;
+#endif
     s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
     s.tile = s.bad ? nullptr : base + un.offset;
     s.count = un.count;
@@ -178,13 +209,20 @@ __device__ __forceinline__ RowSrc param_src(const fp8z1_unit* __restrict__ units
 }
 
 // Run k of a span: elements span_offset + 16384 k .. of param span_param.
-__device__ __forceinline__ RowSrc span_src(const float* const* __restrict__ params, int32_t param,
+__device__ __forceinline__ RowSrc span_src(const float* const* __restrict__ params,
+                                           const int64_t* __restrict__ param_elems, int32_t param,
                                            int64_t offset, int64_t elems, int64_t k)
 {
     const float* base = params[param];
     RowSrc s = {};
     s.bad = base == nullptr || (reinterpret_cast<uintptr_t>(base) & 3) != 0;
     const int64_t o = k * FP8Z1_BLOCK_ELEMS;
+#if FP8Z1_CHECKED
+    s.first = offset + o;
+    s.elems = param_elems[param];
+#else
+    (void)param_elems;
+#endif
     s.tile = s.bad ? nullptr : base + offset + o;
     s.count = (int)(elems - o < FP8Z1_BLOCK_ELEMS ? elems - o : FP8Z1_BLOCK_ELEMS);
     s.vec = !s.bad && (reinterpret_cast<uintptr_t>(s.tile) & 15) == 0;
@@ -196,6 +234,7 @@ struct NormArgs {
     const fp8z1_block* lut;       // kRows
     const fp8z1_unit* units;      // kParams
     const float* const* params;   // kRows, kParams, kSpan: row-major FP32 grads
+    const int64_t* param_elems;   // kRows, kParams, kSpan: each param's extent (checked builds test against it)
     int64_t span_offset;          // kSpan: first element of the span in its param ...
     int64_t span_elems;           // ... its length ...
     int32_t span_param;           // ... and the param
@@ -235,7 +274,9 @@ __device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, in
         if (s.vec && s.count == FP8Z1_BLOCK_ELEMS) {  // a whole, aligned run
             const float4* p = reinterpret_cast<const float4*>(s.tile + e0) + tid;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+            for (int j = 0; j < kVec; ++j)
+                x[j] = src_ok(s, e0 + 4 * (tid + j * kThreads), 4) ? __ldcs(p + j * kThreads)
+                                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             return;
         }
 #pragma unroll
@@ -245,12 +286,12 @@ __device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, in
             if (!s.bad && e < s.count) {
                 const float* src = s.tile + e;
                 if (s.vec && e + 4 <= s.count) {
-                    v = __ldcs(reinterpret_cast<const float4*>(src));
+                    if (src_ok(s, e, 4)) v = __ldcs(reinterpret_cast<const float4*>(src));
                 } else {
-                    v.x = __ldcs(src + 0);
-                    if (e + 1 < s.count) v.y = __ldcs(src + 1);
-                    if (e + 2 < s.count) v.z = __ldcs(src + 2);
-                    if (e + 3 < s.count) v.w = __ldcs(src + 3);
+                    if (src_ok(s, e, 1)) v.x = __ldcs(src + 0);
+                    if (e + 1 < s.count && src_ok(s, e + 1, 1)) v.y = __ldcs(src + 1);
+                    if (e + 2 < s.count && src_ok(s, e + 2, 1)) v.z = __ldcs(src + 2);
+                    if (e + 3 < s.count && src_ok(s, e + 3, 1)) v.w = __ldcs(src + 3);
                 }
             }
             x[j] = v;
@@ -259,10 +300,13 @@ __device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, in
         const int r0 = h * kUnitRows;
         if (s.vec && s.rows == FP8Z1_TILE && s.cols == FP8Z1_TILE) {
             // a full, aligned block: chunk j sits 8 rows below chunk j-1
-            const float* src = s.tile + (int64_t)(r0 + (tid >> 5)) * s.ld + ((tid & 31) << 2);
+            const int64_t off = (int64_t)(r0 + (tid >> 5)) * s.ld + ((tid & 31) << 2);
+            const float* src = s.tile + off;
             const int64_t step = (kThreads / 32) * s.ld;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) x[j] = __ldcs(reinterpret_cast<const float4*>(src + j * step));
+            for (int j = 0; j < kVec; ++j)
+                x[j] = src_ok(s, off + j * step, 4) ? __ldcs(reinterpret_cast<const float4*>(src + j * step))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
             return;
         }
 #pragma unroll
@@ -271,14 +315,15 @@ __device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, in
             const int r = r0 + (ci >> 5), c = (ci & 31) << 2;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (!s.bad && r < s.rows) {
-                const float* src = s.tile + r * s.ld + c;
+                const int64_t off = r * s.ld + c;
+                const float* src = s.tile + off;
                 if (s.vec) {  // a 4-column group is then all real or all padding
-                    if (c < s.cols) v = __ldcs(reinterpret_cast<const float4*>(src));
+                    if (c < s.cols && src_ok(s, off, 4)) v = __ldcs(reinterpret_cast<const float4*>(src));
                 } else {
-                    if (c + 0 < s.cols) v.x = __ldcs(src + 0);
-                    if (c + 1 < s.cols) v.y = __ldcs(src + 1);
-                    if (c + 2 < s.cols) v.z = __ldcs(src + 2);
-                    if (c + 3 < s.cols) v.w = __ldcs(src + 3);
+                    if (c + 0 < s.cols && src_ok(s, off + 0, 1)) v.x = __ldcs(src + 0);
+                    if (c + 1 < s.cols && src_ok(s, off + 1, 1)) v.y = __ldcs(src + 1);
+                    if (c + 2 < s.cols && src_ok(s, off + 2, 1)) v.z = __ldcs(src + 2);
+                    if (c + 3 < s.cols && src_ok(s, off + 3, 1)) v.w = __ldcs(src + 3);
                 }
             }
             x[j] = v;
@@ -291,9 +336,9 @@ template <Src SRC>
 __device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t u)
 {
     const int64_t k = u / kUnitsPerBlock;
-    if (SRC == kRows) return row_src(a.lut, a.params, a.b0 + k);
-    if (SRC == kParams) return param_src(a.units, a.params, a.b0 + k);
-    if (SRC == kSpan) return span_src(a.params, a.span_param, a.span_offset, a.span_elems, k);
+    if (SRC == kRows) return row_src(a.lut, a.params, a.param_elems, a.b0 + k);
+    if (SRC == kParams) return param_src(a.units, a.params, a.param_elems, a.b0 + k);
+    if (SRC == kSpan) return span_src(a.params, a.param_elems, a.span_param, a.span_offset, a.span_elems, k);
     return RowSrc{};
 }
 
@@ -454,6 +499,7 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
     NormArgs a = {};
     a.lut = L->d_lut;
     a.units = L->d_units;
+    a.param_elems = L->d_param_elems;
     a.params = d_grad_params;
     a.store = reinterpret_cast<float4*>(grad_shard);
     a.partials = L->d_partials;
@@ -626,3 +672,5 @@ extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks
     norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();
 }
+
+FP8Z1_CHECKED_MISSES_READER(checked_misses_norm)

@@ -92,6 +92,9 @@ extern "C" int fp8z1_step(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
     a.lut = L->d_lut;
+#if FP8Z1_CHECKED
+    a.param_elems = L->d_param_elems;
+#endif
     a.b0 = b0;
     a.status = L->d_status;
     a.c = scalars(hp);
@@ -138,6 +141,9 @@ int step_fused_impl(const fp8z1_layout* L, const fp8z1_adamw_hp* hp, const fp8z1
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
     a.lut = L->d_lut;
+#if FP8Z1_CHECKED
+    a.param_elems = L->d_param_elems;
+#endif
     a.b0 = b0;
     a.grad_params = d_grad_params;
     a.code_params = d_fp8_params;

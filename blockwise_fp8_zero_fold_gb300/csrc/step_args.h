@@ -51,6 +51,9 @@ struct StepArgs {
     const int32_t* select;       // kSelScalars: c when *select == 0, else c2; the gated forms' flag
     StepScalars c;               // the scalars by value
     StepScalars c2;              // kSelScalars: the other set
+#if FP8Z1_CHECKED
+    const int64_t* param_elems;  // each param's extent, which row-major accesses are tested against
+#endif
 };
 
 // One launch of nb blocks from a.blk_off on; `forms` is an OR of the bits above.

@@ -39,6 +39,7 @@
 
 #include <math.h>
 
+#include "checked.cuh"
 #include "step_args.h"
 
 namespace fp8z1 {
@@ -51,36 +52,40 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// the 4 grads of chunk (r, c) of a row-major tile; zeros outside the real extent
+// The 4 grads of chunk (r, c) of a row-major tile; zeros outside the real
+// extent.  first: the element index of tile[0] in its param, elems: the
+// param's extent (a checked build tests each access against them).
 __device__ __forceinline__ float4 load_grad_rows(const float* tile, int64_t ld, int r, int c, int rows,
-                                                 int cols, bool vec)
+                                                 int cols, bool vec, int64_t first, int64_t elems)
 {
     float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
     if (r < rows) {
+        const int64_t at = first + r * ld + c;
         const float* src = tile + r * ld + c;
         if (vec) {  // ld % 4 == 0: a 4-column group is all real or all padding
-            if (c < cols) g = __ldcs(reinterpret_cast<const float4*>(src));
+            if (c < cols && in_extent(at, 4, elems)) g = __ldcs(reinterpret_cast<const float4*>(src));
         } else {
-            if (c + 0 < cols) g.x = __ldcs(src + 0);
-            if (c + 1 < cols) g.y = __ldcs(src + 1);
-            if (c + 2 < cols) g.z = __ldcs(src + 2);
-            if (c + 3 < cols) g.w = __ldcs(src + 3);
+            if (c + 0 < cols && in_extent(at + 0, 1, elems)) g.x = __ldcs(src + 0);
+            if (c + 1 < cols && in_extent(at + 1, 1, elems)) g.y = __ldcs(src + 1);
+            if (c + 2 < cols && in_extent(at + 2, 1, elems)) g.z = __ldcs(src + 2);
+            if (c + 3 < cols && in_extent(at + 3, 1, elems)) g.w = __ldcs(src + 3);
         }
     }
     return g;
 }
 
 __device__ __forceinline__ void store_codes_rows(uint8_t* tile, int64_t ld, int r, int c, int rows,
-                                                 int cols, bool vec, uint32_t q)
+                                                 int cols, bool vec, uint32_t q, int64_t first, int64_t elems)
 {
     if (r >= rows) return;
+    const int64_t at = first + r * ld + c;
     uint8_t* dst = tile + r * ld + c;
     if (vec) {
-        if (c < cols) __stcs(reinterpret_cast<unsigned int*>(dst), q);
+        if (c < cols && in_extent(at, 4, elems)) __stcs(reinterpret_cast<unsigned int*>(dst), q);
     } else {
 #pragma unroll
         for (int b = 0; b < 4; ++b)
-            if (c + b < cols) dst[b] = (uint8_t)(q >> (8 * b));
+            if (c + b < cols && in_extent(at + b, 1, elems)) dst[b] = (uint8_t)(q >> (8 * b));
     }
 }
 
@@ -106,7 +111,8 @@ __device__ __forceinline__ void monitor_add(float p, float dec, float scale, flo
 template <bool GRAD_ROWS, bool PAD>
 __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, int64_t base,
                                               int tid, const float* gtile, int64_t ld, int rows, int cols,
-                                              bool gvec, float (&pn)[4 * kVec], float& amax)
+                                              bool gvec, int64_t first, int64_t elems, float (&pn)[4 * kVec],
+                                              float& amax)
 {
     const int row0 = tid >> 5, col = (tid & 31) << 2;
     // chunks j < jn hold real elements (rows grow with j, the column does not)
@@ -121,10 +127,13 @@ __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScala
         const int64_t i = base + j * kThreads;
         float4 g4;
         if (GRAD_ROWS) {
-            if (!PAD && gvec)  // a full tile (every launch without PAD), 16-byte rows
-                g4 = __ldcs(reinterpret_cast<const float4*>(gtile + (int64_t)(row0 + 16 * j) * ld + col));
-            else
-                g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec);
+            if (!PAD && gvec) {  // a full tile (every launch without PAD), 16-byte rows
+                const int64_t at = (int64_t)(row0 + 16 * j) * ld + col;
+                g4 = in_extent(first + at, 4, elems) ? __ldcs(reinterpret_cast<const float4*>(gtile + at))
+                                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            } else {
+                g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec, first, elems);
+            }
         } else {
             g4 = __ldcs(a.grad + i);
         }
@@ -170,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     int rows = FP8Z1_TILE, cols = FP8Z1_TILE;
     int64_t ld = 0, off = 0;
     int param = 0;
+    int64_t elems = 0;  // the param's extent (checked builds)
     if (GRAD_ROWS || CODES_ROWS || PAD) {
         const fp8z1_block blk = a.lut[a.b0 + kb];
         rows = blk.rows_real;
@@ -177,6 +187,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         ld = blk.ld;
         off = blk.src_offset;
         param = blk.param;
+#if FP8Z1_CHECKED
+        if (GRAD_ROWS || CODES_ROWS) elems = a.param_elems[param];
+#endif
     }
     const float* gtile = nullptr;
     bool gvec = false;
@@ -210,12 +223,14 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         // one uniform branch, each side with its scalars as kernel-parameter
         // operands (no registers held for them)
         if (s_alt)
-            update_chunks<GRAD_ROWS, PAD>(a, a.c2, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+            update_chunks<GRAD_ROWS, PAD>(a, a.c2, gs, base, tid, gtile, ld, rows, cols, gvec, off, elems, pn,
+                                          amax);
         else
-            update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, base, tid, gtile, ld, rows, cols, gvec, pn, amax);
+            update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, base, tid, gtile, ld, rows, cols, gvec, off, elems, pn,
+                                          amax);
     } else {
         update_chunks<GRAD_ROWS, PAD>(a, SC == kScDevice ? s_c : a.c, gs, base, tid, gtile, ld, rows, cols,
-                                      gvec, pn, amax);
+                                      gvec, off, elems, pn, amax);
     }
 
     amax = warp_max(amax);
@@ -237,10 +252,12 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
         if (CODES_ROWS) {
             const int ci = tid + j * kThreads;
-            if (!PAD && cvec)  // a full tile, 4-byte aligned rows
-                __stcs(reinterpret_cast<unsigned int*>(ctile + (int64_t)(ci >> 5) * ld + ((ci & 31) << 2)), q);
-            else
-                store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q);
+            if (!PAD && cvec) {  // a full tile, 4-byte aligned rows
+                const int64_t at = (int64_t)(ci >> 5) * ld + ((ci & 31) << 2);
+                if (in_extent(off + at, 4, elems)) __stcs(reinterpret_cast<unsigned int*>(ctile + at), q);
+            } else {
+                store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q, off, elems);
+            }
         }
         if (MON) {
             const float2 d01 = e4m3x2_decode(lo), d23 = e4m3x2_decode(hi);

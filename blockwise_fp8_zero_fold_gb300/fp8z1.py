@@ -6,6 +6,11 @@ taken as raw pointers.  ``stream`` is a ``torch.cuda.Stream``, a raw
 ``cudaStream_t`` int, or None for torch's current stream.  A non-zero status
 raises ``Fp8z1Error``.  The library must have been built
 (``__graft_entry__.build()``); there is no fallback.
+
+With ``FP8Z1_CHECKED=1`` in the environment the checked build,
+``libfp8z1_checked.so``, is loaded instead: the same entry points, with every
+row-major param access of its kernels tested against the param's extent
+(``fp8z1_checked_misses`` counts the ones skipped).
 """
 from __future__ import annotations
 
@@ -16,7 +21,9 @@ from typing import Sequence
 
 import numpy as np
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8z1.so")
+CHECKED = os.environ.get("FP8Z1_CHECKED", "0") not in ("", "0")
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                         "libfp8z1_checked.so" if CHECKED else "libfp8z1.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -25,6 +32,7 @@ MX_GROUP = 32
 TILE = 128
 LAYOUT_HOST_ONLY = 1
 DEVSTATUS_BADPTR = 1
+BUILD_CHECKED = 1
 
 OK, EINVAL, EALIGN, ENOMEM, ECUDA, ENODEV = 0, -1, -2, -3, -4, -5
 
@@ -109,6 +117,9 @@ _SIGS = {
     "fp8z1_clip_coef": (C.c_int, [C.c_double, C.c_float, C.c_float, C.POINTER(C.c_double),
                                   C.POINTER(C.c_double)]),
     "fp8z1_kernel_launches": (C.c_int, [C.POINTER(C.c_uint64)]),
+    "fp8z1_build_flags": (C.c_int, []),
+    "fp8z1_checked_misses": (C.c_int, [C.POINTER(C.c_uint64)]),
+    "fp8z1_checked_set_lut_entry": (C.c_int, [_P, C.c_int64, _P]),
     "fp8z1_norm_reset": (C.c_int, [_P, _P, _P]),
     "fp8z1_strerror": (C.c_char_p, [C.c_int]),
 }
@@ -119,12 +130,14 @@ def lib_path() -> str:
 
 
 def lib():
-    """Load libfp8z1.so (raises when it has not been built)."""
+    """Load libfp8z1.so, or libfp8z1_checked.so under FP8Z1_CHECKED=1 (raises
+    when it has not been built)."""
     global _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
-                raise RuntimeError(f"libfp8z1.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+                raise RuntimeError(f"{os.path.basename(_LIB_PATH)} is not built ({_LIB_PATH}); "
+                                   "run __graft_entry__.build()")
             L = C.CDLL(_LIB_PATH)
             for name, (res, args) in _SIGS.items():
                 f = getattr(L, name)
@@ -367,6 +380,25 @@ def fp8z1_kernel_launches() -> int:
     n = C.c_uint64()
     _check(lib().fp8z1_kernel_launches(C.byref(n)), "fp8z1_kernel_launches")
     return n.value
+
+
+def fp8z1_build_flags() -> int:
+    """BUILD_CHECKED for the checked library, else 0."""
+    return int(lib().fp8z1_build_flags())
+
+
+def fp8z1_checked_misses() -> int:
+    """Row-major accesses the checked kernels skipped on the current device
+    (synchronous; 0 in a release build)."""
+    n = C.c_uint64()
+    _check(lib().fp8z1_checked_misses(C.byref(n)), "fp8z1_checked_misses")
+    return n.value
+
+
+def fp8z1_checked_set_lut_entry(layout: Layout, block: int, entry: "fp8z1_block") -> None:
+    """Checked builds' test hook: overwrite one device LUT entry."""
+    _check(lib().fp8z1_checked_set_lut_entry(layout.handle, int(block), C.byref(entry)),
+           "fp8z1_checked_set_lut_entry")
 
 
 def fp8z1_paramwise_split(shapes, dp_size: int):

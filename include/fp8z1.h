@@ -371,6 +371,31 @@ int fp8z1_step_fused_dev(const fp8z1_layout* layout, const fp8z1_step_scalars* h
  * Errors: EINVAL (null). */
 int fp8z1_kernel_launches(uint64_t* out);
 
+/* ---- checked builds --------------------------------------------------------
+ * libfp8z1_checked.so is this library compiled with -DFP8Z1_CHECKED=1: every
+ * load and store a kernel makes to a row-major param (fold and unfold, the
+ * fused norm's grad reads, the fused step's grad reads and code writes) is
+ * first tested against that param's extent, E * R * C elements; an access
+ * outside is skipped and counted instead of made.  It is a debug build, for
+ * running the parity tests without a device memory checker: slower, and
+ * equal to the release build in every result while the count stays 0. */
+#define FP8Z1_BUILD_CHECKED 1u
+
+/* FP8Z1_BUILD_CHECKED for a checked build, else 0. */
+int fp8z1_build_flags(void);
+
+/* The accesses the checked kernels have skipped on the current device since
+ * the library was loaded (synchronous: waits for the device).  0 in a release
+ * build.  Errors: EINVAL (null), ECUDA. */
+int fp8z1_checked_misses(uint64_t* count);
+
+/* Test hook of a checked build: overwrite the device copy of block `block`'s
+ * LUT entry (the host copy is kept), e.g. with an entry that points past its
+ * param, to see the checks skip and count those accesses.  The layout stays
+ * broken until destroyed.  Errors: EINVAL (release build, null, block out of
+ * range), ENODEV, ECUDA. */
+int fp8z1_checked_set_lut_entry(fp8z1_layout* layout, int64_t block, const fp8z1_block* entry);
+
 /* ---- param-wise split (§参数粒度切分; host only) ---------------------------- */
 
 /* The page's alternative to the block-wise split, for comparing padding

@@ -12,7 +12,7 @@ TORCH_OF = {4: torch.float32, 2: torch.int16, 1: torch.uint8}
 
 @pytest.fixture(scope="session")
 def lib():
-    fp8build.build()
+    fp8build.build(checked=F.CHECKED)
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     return F.lib()
 

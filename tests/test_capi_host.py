@@ -44,6 +44,27 @@ def test_exports_every_declared_symbol():
     assert names <= set(F._SIGS), "binding misses a declared entry point"
 
 
+def test_checked_build_exports_and_flags():
+    """The checked variant exports the same symbols and says it is checked;
+    the release build says it is not, reports no misses and refuses the
+    table hook (none of this needs a device)."""
+    path = fp8build.build(checked=True)
+    checked = C.CDLL(path)
+    for n in sorted(_declared()):
+        assert hasattr(checked, n), n
+    checked.fp8z1_build_flags.restype = C.c_int
+    assert checked.fp8z1_build_flags() == F.BUILD_CHECKED
+    release = C.CDLL(fp8build.lib_path(False))
+    release.fp8z1_build_flags.restype = C.c_int
+    assert release.fp8z1_build_flags() == 0
+    n = C.c_uint64(7)
+    assert release.fp8z1_checked_misses(C.byref(n)) == F.OK and n.value == 0
+    assert release.fp8z1_checked_misses(None) == F.EINVAL
+    L = F.fp8z1_build_layout([(1, 128, 128)], host_only=True)
+    e = F.fp8z1_block()
+    assert release.fp8z1_checked_set_lut_entry(C.c_void_p(L.handle), C.c_int64(0), C.byref(e)) == F.EINVAL
+
+
 LUT_CASES = [
     [(1, 300, 200)],
     [(3, 129, 257), (1, 1, 1), (2, 128, 128), (1, 17, 690)],
