@@ -359,22 +359,32 @@ def bench_ours(args, rank, world, dist):
             return opt.step_from_host(hgrads, hfp8, hscales, grads=grads, fp8_params=fp8, wait=wait)
 
         e2e_step(True)
-        if dist is not None:
-            dist.barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step(True)
-        wall_sync = max_over_ranks(time.perf_counter() - t0, dist, dev)
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step(False)
-        opt.finish_host_step()
-        wall = max_over_ranks(time.perf_counter() - t0, dist, dev)
-        e2e = {"value": whole_job_rate(n_pad, world, args.e2e_steps, wall), "unit": "elem/s",
+        # the host link is shared with the machine's other tenants: each form
+        # runs e2e_reps times, the two forms alternating, and the medians count
+        sync_ms, pipe_ms = [], []
+        for _ in range(max(1, args.e2e_reps)):
+            if dist is not None:
+                dist.barrier()
+            t0 = time.perf_counter()
+            for _ in range(args.e2e_steps):
+                e2e_step(True)
+            sync_ms.append(max_over_ranks(time.perf_counter() - t0, dist, dev) / args.e2e_steps * 1e3)
+            if dist is not None:
+                dist.barrier()
+            t0 = time.perf_counter()
+            for _ in range(args.e2e_steps):
+                e2e_step(False)
+            opt.finish_host_step()
+            pipe_ms.append(max_over_ranks(time.perf_counter() - t0, dist, dev) / args.e2e_steps * 1e3)
+        ms = statistics.median(pipe_ms)
+        e2e = {"value": whole_job_rate(n_pad, world, 1, ms / 1e3), "unit": "elem/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": wall / args.e2e_steps * 1e3, "steps": args.e2e_steps,
-               "mode": "steps enqueued back to back (step_from_host wait=False), then finish_host_step",
-               "ms_per_step_one_at_a_time": wall_sync / args.e2e_steps * 1e3}
+               "ms_per_step": ms, "steps": args.e2e_steps, "reps": len(pipe_ms),
+               "mode": "steps enqueued back to back (step_from_host wait=False), then finish_host_step; "
+                       "median of the repetitions",
+               "ms_per_step_reps": pipe_ms,
+               "ms_per_step_one_at_a_time": statistics.median(sync_ms),
+               "ms_per_step_one_at_a_time_reps": sync_ms}
         del hgrads, hfp8
 
     out = {
@@ -693,6 +703,8 @@ def main():
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-reps", type=int, default=3,
+                    help="repetitions of each e2e form (alternating); the medians are reported")
     ap.add_argument("--bf16-fold", type=int, default=0,
                     help="also time N launches each of the bf16 fold and unfold of the weights")
     ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "
