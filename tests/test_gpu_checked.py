@@ -28,7 +28,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # minus the ones that run the bench or link the library from C
 SUITES = ["test_gpu_fold.py", "test_gpu_norm.py", "test_gpu_step.py", "test_gpu_fused.py", "test_gpu_next.py",
           "test_gpu_graph.py", "test_gpu_resume.py", "test_gpu_workloads.py", "test_gpu_maxsize.py",
-          "test_zz_no_alloc.py"]
+          "test_gpu_random_layouts.py", "test_zz_no_alloc.py"]
 
 
 def test_parity_suites_on_the_checked_build(lib):
