@@ -340,6 +340,38 @@ def bench_ours(args, rank, world, dist):
         bf16["bytes_per_launch"] = 2 * (n_real + n_pad)
         del wb, folded
 
+    # the fused step with the per-block quantisation monitors (underflow count
+    # and cosine distortion), and the host-side greedy param-wise split
+    monitors = None
+    if args.monitors:
+        bcos = torch.empty(nblk, dtype=torch.float32, device=dev)
+        bund = torch.empty(nblk, dtype=torch.int32, device=dev)
+
+        def step_mon():
+            hp = F.make_hp(step=opt.scaler.step + 1, loss_scale=opt.scaler.scale, **opt.hp)
+            F.fp8z1_step_fused(opt.layout, hp, d_grad_params=gptrs, master_shard=opt.master,
+                               m_shard=opt.m, v_shard=opt.v, d_fp8_params=fptrs,
+                               scale_shard=opt.scales, block_cos=bcos, block_underflow=bund,
+                               b0=opt.b0, b1=opt.b1, d_sumsq=opt.sumsq, d_found_inf=opt.found_inf)
+
+        for _ in range(3):
+            step_mon()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.monitors)]
+        for a, b in evs:
+            a.record(stream)
+            step_mon()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        t = time.perf_counter()
+        F.fp8z1_paramwise_split(w.shapes, max(dp, 8))
+        split_ms = (time.perf_counter() - t) * 1e3
+        monitors = {"step_ms": ms, "step_gbs": (step_bytes + 8 * nblk) / ms / 1e6,
+                    "bytes_per_launch": step_bytes + 8 * nblk,
+                    "paramwise_split_ms": split_ms, "paramwise_split_dp": max(dp, 8)}
+        del bcos, bund
+
     # e2e: the same step through the public API, grads from pinned host memory
     # and the FP8 weights + scales + found flag read back every step
     e2e = None
@@ -428,6 +460,7 @@ def bench_ours(args, rank, world, dist):
         "e2e": e2e,
         "bf16_fold": bf16,
         "layout_build_ms": layout_ms,
+        "monitors": monitors,
     }
     if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)
@@ -705,6 +738,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--e2e-reps", type=int, default=3,
                     help="repetitions of each e2e form (alternating); the medians are reported")
+    ap.add_argument("--monitors", type=int, default=0,
+                    help="also time N launches of the fused step with the per-block quantisation monitors")
     ap.add_argument("--bf16-fold", type=int, default=0,
                     help="also time N launches each of the bf16 fold and unfold of the weights")
     ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "

@@ -54,7 +54,7 @@ def _check_ours(d, steps):
 @pytest.mark.gpu
 def test_bench_line_tiny():
     d = _run("--workload", "tiny", "--steps", "4", "--warmup", "3", "--compare", "1", "--e2e-steps", "2",
-             "--cpu-sample-experts", "1")
+             "--cpu-sample-experts", "1", "--monitors", "2")
     _check_ours(d, 4)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
@@ -62,6 +62,8 @@ def test_bench_line_tiny():
     assert e["ms_per_step"] == sorted(e["ms_per_step_reps"])[1]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["other_path"]["path"] == "unfused"
+    mon = d["monitors"]
+    assert mon["step_ms"] > 0 and mon["step_gbs"] > 0 and mon["paramwise_split_ms"] >= 0
     lb = d["layout_build_ms"]
     assert 0 < lb["host"] and 0 < lb["host_and_upload"]
     # per step: the flat-run norm, and the step (one launch; two gated ones for a
