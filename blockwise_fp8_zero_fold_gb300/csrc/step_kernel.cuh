@@ -10,13 +10,14 @@
 // then the update, then the low-precision copy; §七: clip_coef = max_norm /
 // (||g_s|| / S + 1e-6), applied when < 1; §六: a found inf skips the step.
 //
-// One CTA of 512 threads per block of 16384 elements; thread t owns the
-// float4 chunks t, t+512, ..., t+3584 of the block (chunk i is row i/32,
-// columns 4*(i%32) .. +3 of the 128x128 block, so a warp covers one block row).
-// It streams grad / master / m / v in, updates them, writes master / m / v back
-// at once and keeps its 32 new master values in registers while the CTA
-// reduces the block amax (warp shuffles, then 16 partials in shared memory).
-// The codes are then produced from the registers: no second pass over HBM.
+// One CTA of 512 threads per block of 16384 elements, three CTAs per SM;
+// thread t owns the float4 chunks t, t+512, ..., t+3584 of the block (chunk i
+// is row i/32, columns 4*(i%32) .. +3 of the 128x128 block, so a warp covers
+// one block row).  It streams grad / master / m / v in, updates them, writes
+// master / m / v back at once and keeps its 32 new master values in its slots
+// of a 64 KB shared array while the CTA reduces the block amax (warp
+// shuffles, then 16 partials in shared memory).  The codes are then produced
+// from shared memory: no second pass over HBM.
 //
 // Where the grads come from and where the codes go is chosen at compile time:
 //   GRAD_ROWS    grads are read from the row-major params through the block
@@ -105,13 +106,22 @@ __device__ __forceinline__ void monitor_add(float p, float dec, float scale, flo
     under += (p != 0.0f && dec == 0.0f) ? 1u : 0u;
 }
 
+// Dynamic shared memory of the kernel: the block's 16384 new masters, which
+// each thread writes to its own slots (chunk j of thread t at t + 512 j) and
+// reads back after the block-amax barrier.  Keeping them there rather than in
+// registers lets three CTAs fit per SM (40 registers) instead of two (64):
+// MoE's full-tile step 6.010 -> 5.894 ms, ragged's padding-aware one 2.806 ->
+// 2.505 ms.  The forms with the quantisation monitors keep two CTAs per SM:
+// their extra sums spilled at 40 registers.
+constexpr int kMasterSmemBytes = kThreads * kVec * 16;
+
 // The update of this thread's 8 float4 chunks of the block: new masters into
-// pn, their largest magnitude into amax.  PAD: skip the chunks that hold
+// pn[j * kThreads] (shared memory), their largest magnitude into amax.  PAD: skip the chunks that hold
 // padding only (chunk j of thread t is row t/32 + 16 j, columns 4 (t%32) .. +3).
 template <bool GRAD_ROWS, bool PAD>
 __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, int64_t base,
                                               int tid, const float* gtile, int64_t ld, int rows, int cols,
-                                              bool gvec, int64_t first, int64_t elems, float (&pn)[4 * kVec],
+                                              bool gvec, int64_t first, int64_t elems, float4* pn,
                                               float& amax)
 {
     const int row0 = tid >> 5, col = (tid & 31) << 2;
@@ -121,7 +131,7 @@ __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScala
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
         if (PAD && j >= jn) {
-            pn[4 * j + 0] = pn[4 * j + 1] = pn[4 * j + 2] = pn[4 * j + 3] = 0.0f;
+            pn[j * kThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
         const int64_t i = base + j * kThreads;
@@ -147,31 +157,36 @@ __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScala
         __stcs(a.mom1 + i, m4);
         __stcs(a.mom2 + i, v4);
         __stcs(a.master + i, p4);
-        pn[4 * j + 0] = p4.x;
-        pn[4 * j + 1] = p4.y;
-        pn[4 * j + 2] = p4.z;
-        pn[4 * j + 3] = p4.w;
+        pn[j * kThreads] = p4;
         amax = fmaxf(amax, fmaxf(fmaxf(fabsf(p4.x), fabsf(p4.y)), fmaxf(fabsf(p4.z), fabsf(p4.w))));
     }
 }
 
 template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, int SC, bool PAD>
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
+__global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
     if (SC == kScGateClear || SC == kScGateSet) {
         if ((*a.select != 0) != (SC == kScGateSet)) return;  // the other set's launch does the step
     }
+    // Where the update reads its scalars: shared memory for the scalars from
+    // device memory, and for the by-value full-tile forms that read the grads
+    // row-major -- at 40 registers those spilled reading the parameters at
+    // every use (MoE: 6.010 -> 5.907 ms from shared memory); the kernel
+    // parameters for the rest, whose issue-bound padding-aware and folded
+    // forms ran up to 9% slower with the extra shared-memory loads.  The select
+    // form keeps its two sets as parameters behind one uniform branch.
+    constexpr bool kSmemScalars = SC == kScDevice || (SC != kScSelect && GRAD_ROWS && !PAD);
     __shared__ float s_gscale;
     __shared__ float s_amax[kWarps];
     __shared__ StepScalars s_c;
     __shared__ int s_alt;
     const int tid = threadIdx.x;
     if (tid == 0) {
-        if (SC == kScDevice) s_c = *a.dsc;
+        if (kSmemScalars) s_c = SC == kScDevice ? *a.dsc : a.c;
         const bool alt = SC == kScSelect && *a.select != 0;
         s_alt = alt;
-        s_gscale = grad_factor(*a.sumsq, SC == kScDevice ? s_c : (alt ? a.c2 : a.c));
+        s_gscale = grad_factor(*a.sumsq, kSmemScalars ? s_c : (alt ? a.c2 : a.c));
     }
 
     // the block's place in its row-major param and its real extent
@@ -217,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     const float gs = s_gscale;
 
     const int64_t base = kb * (FP8Z1_BLOCK_ELEMS / 4) + tid;
-    float pn[4 * kVec];
+    extern __shared__ float4 s_pn[];  // kMasterSmemBytes: the block's new masters
+    float4* const pn = s_pn + tid;
     float amax = 0.0f;
     if constexpr (SC == kScSelect) {
         // one uniform branch, each side with its scalars as kernel-parameter
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
             update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, base, tid, gtile, ld, rows, cols, gvec, off, elems, pn,
                                           amax);
     } else {
-        update_chunks<GRAD_ROWS, PAD>(a, SC == kScDevice ? s_c : a.c, gs, base, tid, gtile, ld, rows, cols,
+        update_chunks<GRAD_ROWS, PAD>(a, kSmemScalars ? s_c : a.c, gs, base, tid, gtile, ld, rows, cols,
                                       gvec, off, elems, pn, amax);
     }
 
@@ -246,8 +262,9 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
     uint32_t under = 0u;
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-        const uint32_t lo = e4m3x2(__fdiv_rn(pn[4 * j + 0], scale), __fdiv_rn(pn[4 * j + 1], scale));
-        const uint32_t hi = e4m3x2(__fdiv_rn(pn[4 * j + 2], scale), __fdiv_rn(pn[4 * j + 3], scale));
+        const float4 p = pn[j * kThreads];
+        const uint32_t lo = e4m3x2(__fdiv_rn(p.x, scale), __fdiv_rn(p.y, scale));
+        const uint32_t hi = e4m3x2(__fdiv_rn(p.z, scale), __fdiv_rn(p.w, scale));
         const uint32_t q = lo | (hi << 16);
         if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
         if (CODES_ROWS) {
@@ -261,10 +278,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const StepArgs a)
         }
         if (MON) {
             const float2 d01 = e4m3x2_decode(lo), d23 = e4m3x2_decode(hi);
-            monitor_add(pn[4 * j + 0], d01.x, scale, pd, pp, dd, under);
-            monitor_add(pn[4 * j + 1], d01.y, scale, pd, pp, dd, under);
-            monitor_add(pn[4 * j + 2], d23.x, scale, pd, pp, dd, under);
-            monitor_add(pn[4 * j + 3], d23.y, scale, pd, pp, dd, under);
+            monitor_add(p.x, d01.x, scale, pd, pp, dd, under);
+            monitor_add(p.y, d01.y, scale, pd, pp, dd, under);
+            monitor_add(p.z, d23.x, scale, pd, pp, dd, under);
+            monitor_add(p.w, d23.y, scale, pd, pp, dd, under);
         }
     }
     if (MON) {
@@ -320,7 +337,11 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
                   (MON ? kMonitors : 0u) | (SCAL == kScDevice ? kDevScalars : 0u) |                   \
                   (SCAL == kScSelect ? kSelScalars : 0u) | (SCAL == kScGateClear ? kGateClear : 0u) |  \
                   (SCAL == kScGateSet ? kGateSet : 0u))) {                                           \
-        step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, 0, s>>>(a);                \
+        static const bool smem_ok = cudaFuncSetAttribute(step_kernel<GR, CR, CF, MON, SCAL, PAD>,      \
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,  \
+                                                         kMasterSmemBytes) == cudaSuccess;             \
+        (void)smem_ok;                                                                               \
+        step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, kMasterSmemBytes, s>>>(a);  \
         return;                                                                                      \
     }
 #define FP8Z1_STEP_FORMS_GC(GR, CR, CF)                                                              \
