@@ -111,8 +111,9 @@ __device__ __forceinline__ void monitor_add(float p, float dec, float scale, flo
 // reads back after the block-amax barrier.  Keeping them there rather than in
 // registers lets three CTAs fit per SM (40 registers) instead of two (64):
 // MoE's full-tile step 6.010 -> 5.894 ms, ragged's padding-aware one 2.806 ->
-// 2.505 ms.  The forms with the quantisation monitors keep two CTAs per SM:
-// their extra sums spilled at 40 registers.
+// 2.505 ms.  The forms with the quantisation monitors keep two CTAs per SM
+// (up to 64 registers): squeezed to 40 with three, their extra sums ran 9%
+// slower on MoE (7.37 against 6.78 ms).
 constexpr int kMasterSmemBytes = kThreads * kVec * 16;
 
 // The update of this thread's 8 float4 chunks of the block: new masters into
