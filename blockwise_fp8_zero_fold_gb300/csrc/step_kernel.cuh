@@ -40,6 +40,8 @@
 
 #include <math.h>
 
+#include <atomic>
+
 #include "checked.cuh"
 #include "step_args.h"
 
@@ -326,6 +328,25 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
 
 // `hp` may be null (scalars in device memory); when given it must be in domain
 
+// Lets `kernel` take kMasterSmemBytes of dynamic shared memory on the current
+// device (an attribute set per device), once per device; a failure shows as
+// the launch's error.
+inline void allow_master_smem(const void* kernel, std::atomic<uint64_t>& set)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return;
+    }
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (set.load(std::memory_order_relaxed) & bit)) return;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMasterSmemBytes) ==
+        cudaSuccess)
+        set.fetch_or(bit, std::memory_order_relaxed);
+    else
+        cudaGetLastError();
+}
+
 template <bool PAD>
 void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
 {
@@ -338,10 +359,8 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
                   (MON ? kMonitors : 0u) | (SCAL == kScDevice ? kDevScalars : 0u) |                   \
                   (SCAL == kScSelect ? kSelScalars : 0u) | (SCAL == kScGateClear ? kGateClear : 0u) |  \
                   (SCAL == kScGateSet ? kGateSet : 0u))) {                                           \
-        static const bool smem_ok = cudaFuncSetAttribute(step_kernel<GR, CR, CF, MON, SCAL, PAD>,      \
-                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,  \
-                                                         kMasterSmemBytes) == cudaSuccess;             \
-        (void)smem_ok;                                                                               \
+        static std::atomic<uint64_t> smem_set{0}; /* devices whose attribute is set */                  \
+        allow_master_smem(reinterpret_cast<const void*>(&step_kernel<GR, CR, CF, MON, SCAL, PAD>), smem_set); \
         step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, kMasterSmemBytes, s>>>(a);  \
         return;                                                                                      \
     }
