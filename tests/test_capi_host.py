@@ -44,6 +44,22 @@ def test_exports_every_declared_symbol():
     assert names <= set(F._SIGS), "binding misses a declared entry point"
 
 
+def test_checked_env_selects_checked_library():
+    """FP8Z1_CHECKED=1 makes the binding load libfp8z1_checked.so (and only
+    then); its build flags say so.  No device is needed."""
+    import subprocess
+    import sys
+    fp8build.build(checked=True)
+    code = ("from blockwise_fp8_zero_fold_gb300 import fp8z1 as F; "
+            "print(F.CHECKED, F.lib_path().endswith('libfp8z1_checked.so'), F.fp8z1_build_flags())")
+    for env_value, want in (("1", "True True 1"), ("0", "False False 0")):
+        env = dict(os.environ, FP8Z1_CHECKED=env_value)
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                           timeout=120)
+        assert r.returncode == 0, r.stderr
+        assert r.stdout.split()[-3:] == want.split(), r.stdout
+
+
 def test_checked_build_exports_and_flags():
     """The checked variant exports the same symbols and says it is checked;
     the release build says it is not, reports no misses and refuses the
