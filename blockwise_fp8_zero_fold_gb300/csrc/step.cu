@@ -39,23 +39,11 @@ void launch_segments(const fp8z1_layout* L, StepArgs a, int64_t b0, int64_t b1, 
 {
     auto one = [&](int64_t k0, int64_t k1, bool pad) {
         a.blk_off = k0 - b0;
-        if (!pad) {
-            fp8z1::count_launch();
-            launch<false>(a, k1 - k0, s, forms);
-        } else if (!(forms & kSelScalars)) {
-            fp8z1::count_launch();
+        fp8z1::count_launch();
+        if (pad)
             launch<true>(a, k1 - k0, s, forms);
-        } else {
-            // the padding-aware select form would spill: two gated by-value
-            // launches instead, of which the flag lets one do the step
-            const unsigned base = forms & ~kSelScalars;
-            fp8z1::count_launch();
-            launch<true>(a, k1 - k0, s, base | kGateClear);
-            StepArgs b = a;
-            b.c = a.c2;
-            fp8z1::count_launch();
-            launch<true>(b, k1 - k0, s, base | kGateSet);
-        }
+        else
+            launch<false>(a, k1 - k0, s, forms);
     };
     int64_t k = b0;
     for (size_t r = 0; r + 1 < L->full_runs.size() && k < b1; r += 2) {

@@ -21,14 +21,10 @@ enum : unsigned {
     kMonitors = 8u,     // per-block underflow count and cosine
     kDevScalars = 16u,  // step scalars read from device memory
     kSelScalars = 32u,  // two scalar sets by value, picked by a device flag
-    kGateClear = 64u,   // by value, run only when the device flag is 0
-    kGateSet = 128u,    // by value, run only when the device flag is not 0
 };
 
-// where the kernel takes its step scalars from; the gated forms are two
-// by-value launches of which the flag lets one run (padding-aware runs, where
-// the select form would spill)
-enum ScalarSource : int { kScValue = 0, kScDevice = 1, kScSelect = 2, kScGateClear = 3, kScGateSet = 4 };
+// where the kernel takes its step scalars from
+enum ScalarSource : int { kScValue = 0, kScDevice = 1, kScSelect = 2 };
 
 struct StepArgs {
     const float4* grad;          // folded grad shard (!kGradRows)
@@ -48,7 +44,7 @@ struct StepArgs {
     float* block_cos;            // kMonitors: cosine(master, dequantised) per block
     uint32_t* block_underflow;   // kMonitors: non-zero masters whose code is 0, per block
     const StepScalars* dsc;      // kDevScalars: the scalars in device memory
-    const int32_t* select;       // kSelScalars: c when *select == 0, else c2; the gated forms' flag
+    const int32_t* select;       // kSelScalars: c when *select == 0, else c2
     StepScalars c;               // the scalars by value
     StepScalars c2;              // kSelScalars: the other set
 #if FP8Z1_CHECKED

@@ -169,9 +169,6 @@ template <bool GRAD_ROWS, bool CODES_ROWS, bool CODES_FOLDED, bool MON, int SC, 
 __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepArgs a)
 {
     if (*a.found_inf != 0) return;  // skipped step: write nothing
-    if (SC == kScGateClear || SC == kScGateSet) {
-        if ((*a.select != 0) != (SC == kScGateSet)) return;  // the other set's launch does the step
-    }
     // Where the update reads its scalars: shared memory for the scalars from
     // device memory, and for the by-value full-tile forms that read the grads
     // row-major -- at 40 registers those spilled reading the parameters at
@@ -357,8 +354,7 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
 #define FP8Z1_STEP_FORM(GR, CR, CF, MON, SCAL)                                                       \
     if (forms == ((GR ? kGradRows : 0u) | (CR ? kCodesRows : 0u) | (CF ? kCodesFolded : 0u) |         \
                   (MON ? kMonitors : 0u) | (SCAL == kScDevice ? kDevScalars : 0u) |                   \
-                  (SCAL == kScSelect ? kSelScalars : 0u) | (SCAL == kScGateClear ? kGateClear : 0u) |  \
-                  (SCAL == kScGateSet ? kGateSet : 0u))) {                                           \
+                  (SCAL == kScSelect ? kSelScalars : 0u))) {                                          \
         static std::atomic<uint64_t> smem_set{0}; /* devices whose attribute is set */                  \
         allow_master_smem(reinterpret_cast<const void*>(&step_kernel<GR, CR, CF, MON, SCAL, PAD>), smem_set); \
         step_kernel<GR, CR, CF, MON, SCAL, PAD><<<(unsigned)nb, kThreads, kMasterSmemBytes, s>>>(a);  \
@@ -369,12 +365,7 @@ void launch(const StepArgs& a, int64_t nb, cudaStream_t s, unsigned forms)
     FP8Z1_STEP_FORM(GR, CR, CF, false, kScDevice)                                                    \
     FP8Z1_STEP_FORM(GR, CR, CF, true, kScValue)                                                      \
     FP8Z1_STEP_FORM(GR, CR, CF, true, kScDevice)                                                     \
-    if (!PAD) {                                                                                      \
-        FP8Z1_STEP_FORM(GR, CR, CF, false, kScSelect)                                                \
-    } else {                                                                                         \
-        FP8Z1_STEP_FORM(GR, CR, CF, false, kScGateClear)                                             \
-        FP8Z1_STEP_FORM(GR, CR, CF, false, kScGateSet)                                               \
-    }
+    FP8Z1_STEP_FORM(GR, CR, CF, false, kScSelect)
     FP8Z1_STEP_FORMS_GC(true, true, true)
     FP8Z1_STEP_FORMS_GC(true, true, false)
     FP8Z1_STEP_FORMS_GC(true, false, true)
