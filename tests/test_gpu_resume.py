@@ -168,12 +168,20 @@ def test_unit_scale_blocks_counts_zero_blocks(lib):
     assert opt.stats()["unit_scale_blocks"] == 2
 
 
-def test_async_steps_equal_synchronous_steps(lib):
+# padded runs only (36 full tiles are too few for a full-tile run); and a
+# 512-block full-tile param between padded ones, so that each step is a
+# full-tile launch and padded launches, each picking its scalars by the flag
+ASYNC_SHAPES = {"padded": [(3, 512, 384), (1, 1000, 131), (2, 130, 260)],
+                "full_and_padded": [(1, 1000, 131), (1, 4096, 2048), (2, 130, 260)]}
+
+
+@pytest.mark.parametrize("layout_kind", list(ASYNC_SHAPES))
+def test_async_steps_equal_synchronous_steps(lib, layout_kind):
     """Eight steps enqueued ahead of their found_inf (launch_step_async: each
     step's t and S picked on the device by the previous step's flag), with
     skips at steps 3, 4 and 7 and the scale growing every 2 clean steps: the
     state, FP8 weights, scales and loss scaler equal the synchronous path's."""
-    w = synth.workload("tiny", shapes=[(3, 512, 384), (1, 1000, 131), (2, 130, 260)], dp=1, rank=0,
+    w = synth.workload("tiny", shapes=ASYNC_SHAPES[layout_kind], dp=1, rank=0,
                        m_sigma=1e-4, v_sigma=1e-8, max_norm=0.5)
     sync, asy = _make(w, 0), _make(w, 0)
     for o in (sync, asy):
