@@ -139,6 +139,19 @@ int main()
 
     uint64_t launches = 1;
     EXPECT(fp8z1_kernel_launches(&launches) == FP8Z1_OK && launches == 0);
+    // the release build's checked-build entry points: flags 0, no misses, no table hook
+    EXPECT(fp8z1_build_flags() == 0);
+    uint64_t misses = 7;
+    EXPECT(fp8z1_checked_misses(&misses) == FP8Z1_OK && misses == 0);
+    EXPECT(fp8z1_checked_misses(nullptr) == FP8Z1_EINVAL);
+    {
+        const fp8z1_shape one = {1, 128, 128};
+        fp8z1_layout* L = nullptr;
+        EXPECT(fp8z1_build_layout(&one, 1, 1, FP8Z1_LAYOUT_HOST_ONLY, &L) == FP8Z1_OK);
+        fp8z1_block e = {};
+        EXPECT(fp8z1_checked_set_lut_entry(L, 0, &e) == FP8Z1_EINVAL);
+        EXPECT(fp8z1_destroy_layout(L) == FP8Z1_OK);
+    }
     for (int st = 1; st >= -9; --st) EXPECT(fp8z1_strerror(st) != nullptr);
     std::printf("layout driver ok\n");
     return 0;
