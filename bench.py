@@ -715,6 +715,32 @@ def bench_reference(args, rank, world):
     }
 
 
+WORKLOADS = ("tiny", "dense", "moe", "ragged", "large", "large_literal")
+
+
+def list_workloads():
+    """One JSON line per workload: its shapes (or the rule that draws them),
+    sizes, hyper-parameters and input distributions, as synth.py defines them."""
+    import dataclasses
+
+    sys.path.insert(0, ROOT)
+    from blockwise_fp8_zero_fold_gb300 import synth
+
+    for name in WORKLOADS:
+        w = synth.workload(name)
+        d = dataclasses.asdict(w)
+        shapes = [tuple(int(x) for x in s) for s in w.shapes]
+        d["n_params"] = len(shapes)
+        d["n_blocks"] = sum(e * -(-r // 128) * -(-c // 128) for e, r, c in shapes)
+        d["n_real"] = w.n_real
+        if name == "ragged":
+            d["shapes"] = "synth.ragged_shapes(n=4000, lo=17, hi=690, seed=0): R, C uniform in [17, 690], " \
+                          "redrawn while a multiple of 128"
+        else:
+            d["shapes"] = shapes
+        print(json.dumps(d))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -746,7 +772,12 @@ def main():
                     "instead of the whole buffer (block scheme)")
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=1)
+    ap.add_argument("--list-workloads", action="store_true",
+                    help="print each workload's configuration as one JSON line and exit")
     args = ap.parse_args()
+    if args.list_workloads:
+        list_workloads()
+        return
     if args.pipeline < 0:
         args.pipeline = int(args.scheme == "mx" or args.path == "fused")
     if args.warmup < 3 and args.impl == "ours":

@@ -37,6 +37,19 @@ def test_reference_arm_line():
     assert "workload" in d["config"]
 
 
+def test_list_workloads():
+    """Every workload's configuration as JSON (no device needed), with the
+    block counts of the configurations the workloads stand for."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--list-workloads"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    got = {d["name"]: d for d in map(json.loads, r.stdout.splitlines())}
+    assert {k: v["n_blocks"] for k, v in got.items()} == {
+        "tiny": 6, "dense": 15040, "moe": 86016, "ragged": 42706, "large": 244608, "large_literal": 204288}
+    assert got["moe"]["n_real"] == 1409286144 and (got["moe"]["dp"], got["moe"]["rank"]) == (8, 3)
+    assert got["ragged"]["n_params"] == 4000 and got["ragged"]["inf_step"] == 2
+
+
 def _check_ours(d, steps):
     assert BASE_KEYS <= set(d) and "impl" not in d
     assert d["value"] > 0 and d["steps"] == steps and d["warmup"] >= 3
