@@ -134,6 +134,29 @@ def _workload(args, synth):
     return w if shapes == w.shapes else synth.workload(args.workload, dp=1, rank=0, shapes=shapes)
 
 
+def _config(args, shapes, dp, shard_rank, b0, b1, n_real, world) -> dict:
+    """The workload the line measures; both arms report this same record."""
+    whole = dp == 1
+    return {
+        "workload": _workload_label(args, shapes),
+        "blocks": b1 - b0, "elems_padded": (b1 - b0) * 16384, "elems_real": n_real,
+        "dp": "whole buffer (1 rank)" if whole else
+              f"rank {shard_rank} of {dp}: blocks [{b0}, {b1}) (this rank's norm partial; no all-reduce on one GPU)",
+        "parallelism": f"replicas{world}" if world > 1 else "single",
+        "l2": _l2_note(b1 - b0, n_real),
+        "value_counts": "padded elements per second through the whole step",
+    }
+
+
+def _l2_note(nblk, n_real) -> str:
+    """How the timed steps avoid L2 reuse: the state a fused step touches
+    (master / m / v folded, grads and FP8 weights row-major) against L2."""
+    gb = (12 * nblk * 16384 + 5 * (n_real or nblk * 16384)) / 1e9
+    if gb > 0.129 * 4:
+        return f"inputs larger than L2 (~{gb:.0f} GB resident per step), no flush"
+    return f"inputs ({gb * 1e3:.1f} MB) fit in L2: a latency-bound case, not a bandwidth figure"
+
+
 def _time_layout_build(F, shapes, dp, reps=3):
     """Host wall time of the one-time layout build (block table, run table,
     shard ranges) and of the build plus its upload to the device; medians."""
@@ -197,6 +220,7 @@ def bench_ours(args, rank, world, dist):
     lut = F.fp8z1_copy_lut(opt.layout)[opt.b0:opt.b1]
     n_real = int((lut["rows_real"].astype("int64") * lut["cols_real"].astype("int64")).sum())
     whole = (opt.b0, opt.b1) == (0, opt.nblk)
+    b0, b1 = opt.b0, opt.b1
 
     def stages(path):
         """The kernels of one step on ``path``, as (label, launch) pairs."""
@@ -310,10 +334,13 @@ def bench_ours(args, rank, world, dist):
     gbs["step"] = achieved
     tr = _ncu_traffic()
     traffic = None
+    traffic_basis = None
     if tr and tr.get("workload") == args.workload and tr.get("path") == args.path and \
             bool(tr.get("pipelined")) == bool(args.pipeline and args.path == "fused") and \
             tr.get("source_sha") == _step_source_sha() and not args.experts and not args.params and whole:
         traffic = tr.get("bytes_per_launch")
+        traffic_basis = (f"extrapolated: ncu DRAM read + write of {tr.get('captured_on')}, "
+                         f"scaled {tr.get('scale')}")
 
     # bf16 fold / unfold of the weights over the shard (2-byte elements)
     bf16 = None
@@ -419,6 +446,16 @@ def bench_ours(args, rank, world, dist):
                "ms_per_step_one_at_a_time_reps": sync_ms}
         del hgrads, hfp8
 
+    # the other configurations, each a few steps of the same loop, after the
+    # headline's timed region (its buffers freed first)
+    others = None
+    if args.other_workloads and not args.experts and not args.params:
+        del opt, grads, fp8, gptrs, fptrs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        others = [other_workload(spec, args.other_steps, dev, dist, peak) for spec in
+                  args.other_workloads.split(",") if spec]
+
     out = {
         "metric": METRIC,
         "value": value,
@@ -432,14 +469,7 @@ def bench_ours(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
-        "config": {
-            "workload": _workload_label(args, w.shapes),
-            "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "dp": "whole buffer (1 rank)" if whole else
-                  f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1}) (this rank's norm partial; no all-reduce on one GPU)",
-            "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": "inputs larger than L2 (~31 GB resident per step), no flush",
-            "value_counts": "padded elements per second through the whole step",
-        },
+        "config": _config(args, w.shapes, dp, shard_rank, b0, b1, n_real, world),
         "gpu_launches": launches,
         "path": args.path,
         "pipelined": bool(args.pipeline and args.path == "fused"),
@@ -450,7 +480,7 @@ def bench_ours(args, rank, world, dist):
         "kernels_ms_median": kern_med,
         "real_elem_per_s": whole_job_rate(n_real, world, args.steps, elapsed_ms / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
+                     "frac": achieved / peak, "traffic": traffic, "traffic_basis": traffic_basis,
                      "kernel": ("fp8z1_step_fused_select" if args.pipeline else "fp8z1_step_fused")
                                if args.path == "fused" else "fp8z1_step",
                      "peak_source": peak_kind,
@@ -461,10 +491,85 @@ def bench_ours(args, rank, world, dist):
         "bf16_fold": bf16,
         "layout_build_ms": layout_ms,
         "monitors": monitors,
+        "other_workloads": others,
     }
     if rank == 0 and world == 1 and args.cpu_sample_experts > 0:
         out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample_experts)
         out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(args.workload, args.cpu_sample_experts)
+    return out
+
+
+def other_workload(spec: str, steps: int, dev, dist, peak: float) -> dict:
+    """One more configuration in the headline's loop (fused path, each step
+    enqueued before the previous one's found_inf is read), ``steps`` timed
+    steps after 3 warm-up steps.  ``spec`` is a workload name, optionally
+    with ``@D:r`` for DP rank r of D's block range.  Reports the whole step
+    and each kernel (CUDA events on the launching stream), their bytes per
+    real element as GB/s and as a fraction of the measured copy bandwidth."""
+    import torch
+
+    from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
+    from blockwise_fp8_zero_fold_gb300 import synth
+    from blockwise_fp8_zero_fold_gb300.optimizer import ShardOptimizer
+
+    name, _, shard = spec.partition("@")
+    dp, shard_rank = (int(x) for x in shard.split(":")) if shard else (1, 0)
+    w = synth.workload(name, dp=dp, rank=shard_rank)
+    t_setup = time.perf_counter()
+    opt = ShardOptimizer(w.shapes, dp_size=dp, rank=shard_rank, device=dev, loss_scale=w.loss_scale,
+                         growth_interval=w.growth_interval,
+                         **{k: v for k, v in w.hp().items() if k != "loss_scale"})
+    for kind in ("master", "m", "v"):
+        if {"master": w.master_sigma, "m": w.m_sigma, "v": w.v_sigma}[kind] == 0.0 and not w.zero_tile_frac:
+            continue  # the optimizer's buffers start at zero
+        rm = synth.make_state(w, kind, dev)
+        opt.fold_into(rm, getattr(opt, kind))
+        del rm
+    grads = synth.make_grads(w, 1, dev)
+    fp8 = [torch.zeros(s, dtype=torch.uint8, device=dev) for s in w.shapes]
+    gptrs, fptrs = opt.pointers(grads), opt.pointers(fp8)
+    nblk = opt.b1 - opt.b0
+    lut = F.fp8z1_copy_lut(opt.layout)[opt.b0:opt.b1]
+    n_real = int((lut["rows_real"].astype("int64") * lut["cols_real"].astype("int64")).sum())
+    n_pad = nblk * F.BLOCK_ELEMS
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        opt.launch_step_async(gptrs, fptrs, stream)
+    opt.drain()
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)] for k in ("norm", "step")}
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    skipped = 0
+    for i in range(steps):
+        skipped += sum(opt.launch_step_async(gptrs, fptrs, stream, {"norm": ev["norm"][i], "step": ev["step"][i]}))
+    skipped += sum(opt.drain())
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev) / steps
+    kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    step_bytes = STEP_BYTES_PER_ELEM * n_real + STEP_BYTES_PER_BLOCK * nblk
+    norm_bytes = 4 * n_real
+    gbs = {"norm": norm_bytes / kern["norm"] / 1e6, "step": step_bytes / kern["step"] / 1e6}
+    out = {"workload": _workload_label(argparse.Namespace(workload=name, experts=0, params=0), w.shapes),
+           "dp": "whole buffer (1 rank)" if dp == 1 else f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1})",
+           "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "steps": steps, "warmup": 3,
+           "ms_per_step": ms, "value": n_pad / (ms / 1e3), "real_elem_per_s": n_real / (ms / 1e3),
+           "kernels_ms": {"fold_norm": kern["norm"], "step": kern["step"]},
+           "kernels_ms_median": {"fold_norm": med["norm"], "step": med["step"]},
+           "bytes_per_launch": {"fold_norm": norm_bytes, "step": step_bytes},
+           "kernels_gbs": {"fold_norm": gbs["norm"], "step": gbs["step"]},
+           "frac_of_measured": {"fold_norm": gbs["norm"] / peak, "step": gbs["step"] / peak},
+           "skipped_steps": skipped, "setup_s": setup_s}
+    del opt, grads, fp8, gptrs, fptrs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return out
 
 
@@ -661,11 +766,15 @@ def _host_info():
     return {"cpu": _cpu_name(), "host_cores": os.cpu_count(), "ram_gb": ram}
 
 
-def cpu_baseline(workload: str, experts: int):
+def cpu_baseline(workload: str, experts: int, min_seconds: float = 10.0):
+    """The oracle on one core: passes over the sample until min_seconds of CPU
+    work have run (at least two)."""
     s = OracleSample(workload, experts)
-    t = s.run()
-    return {"value": s.n_pad / t, "unit": "elem/s", "cores": 1, "kind": "oracle",
-            "sample": s.sample, "seconds": t, **_host_info()}
+    ts = []
+    while len(ts) < 2 or sum(ts) < min_seconds:
+        ts.append(s.run())
+    return {"value": s.n_pad * len(ts) / sum(ts), "unit": "elem/s", "cores": 1, "kind": "oracle",
+            "sample": s.sample, "passes": len(ts), "seconds": sum(ts), **_host_info()}
 
 
 def cpu_baseline_all_cores(workload: str, experts: int):
@@ -695,27 +804,53 @@ def _cpu_name():
 
 
 def bench_reference(args, rank, world):
-    """The oracle as the reference arm, on the host cores, rank 0 only."""
+    """The oracle as the reference arm, on the host cores, rank 0 only: the
+    same workload record as our arm's line, each step one pass of the oracle
+    over a bounded sample -- the cpu_baseline's sample (the first
+    --cpu-sample-experts experts of each param) unless the run's W + K passes
+    would then exceed --ref-budget-s, in which case fewer experts."""
     if rank != 0:
         return None
-    smp = OracleSample(args.workload, args.ref_sample_experts)
-    for _ in range(args.warmup):
+    from blockwise_fp8_zero_fold_gb300 import synth
+
+    experts = args.ref_sample_experts if args.ref_sample_experts > 0 else max(1, args.cpu_sample_experts)
+    smp = OracleSample(args.workload, experts)
+    first = smp.run()  # the first warm-up pass, also sizing the sample
+    passes = args.warmup + args.steps
+    if args.ref_sample_experts <= 0 and passes * first > args.ref_budget_s and experts > 1:
+        experts = max(1, int(experts * args.ref_budget_s / (passes * first)))
+        smp = OracleSample(args.workload, experts)
+        smp.run()
+    for _ in range(args.warmup - 1):
         smp.run()
     ts = [smp.run() for _ in range(args.steps)]
     v = smp.n_pad * len(ts) / sum(ts)
+    w = _workload(args, synth)
+    dp, shard_rank = (int(x) for x in args.shard.split(":")) if args.shard else (1, 0)
+    nblk = sum(e * -(-r // 128) * -(-c // 128) for e, r, c in w.shapes)
+    per = -(-nblk // dp)
+    b0, b1 = min(per * shard_rank, nblk), min(per * (shard_rank + 1), nblk)
+    if dp == 1:
+        n_real = w.n_real
+    else:
+        import oracle
+        lut = oracle.build_lut(w.shapes)[b0:b1]
+        n_real = int((lut[:, 4] * lut[:, 5]).sum())
     return {
         "impl": "reference",
         "metric": METRIC, "value": v, "unit": "elem/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sum(ts) / len(ts) * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload} (oracle on a bounded sample: {smp.sample})"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,s) grads/master/moments as the workload states)",
+        "config": _config(args, w.shapes, dp, shard_rank, b0, b1, n_real, world),
+        "sample": smp.sample,
         "cpu_baseline": {"value": v, "unit": "elem/s", "cores": 1, "kind": "oracle",
                          "sample": smp.sample, **_host_info()},
         "e2e": {"value": v, "unit": "elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-WORKLOADS = ("tiny", "dense", "moe", "ragged", "large", "large_literal")
+WORKLOADS = ("tiny", "dense", "moe", "ragged", "ragged_literal", "large", "large_literal")
 
 
 def list_workloads():
@@ -733,8 +868,9 @@ def list_workloads():
         d["n_params"] = len(shapes)
         d["n_blocks"] = sum(e * -(-r // 128) * -(-c // 128) for e, r, c in shapes)
         d["n_real"] = w.n_real
-        if name == "ragged":
-            d["shapes"] = "synth.ragged_shapes(n=4000, lo=17, hi=690, seed=0): R, C uniform in [17, 690], " \
+        if name in ("ragged", "ragged_literal"):
+            hi = 690 if name == "ragged" else 3000
+            d["shapes"] = f"synth.ragged_shapes(n=4000, lo=17, hi={hi}, seed=0): R, C uniform in [17, {hi}], " \
                           "redrawn while a multiple of 128"
         else:
             d["shapes"] = shapes
@@ -770,8 +906,15 @@ def main():
                     help="also time N launches each of the bf16 fold and unfold of the weights")
     ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "
                     "instead of the whole buffer (block scheme)")
+    ap.add_argument("--other-workloads", default="dense,ragged,moe@8:3,ragged_literal",
+                    help="comma-separated configurations (name or name@D:r) timed after the headline "
+                         "for --other-steps steps each in the same loop; empty: none")
+    ap.add_argument("--other-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
-    ap.add_argument("--ref-sample-experts", type=int, default=1)
+    ap.add_argument("--ref-sample-experts", type=int, default=0,
+                    help="experts per param in the reference arm's sample; 0: the cpu_baseline's, "
+                         "fewer when W + K passes would exceed --ref-budget-s")
+    ap.add_argument("--ref-budget-s", type=float, default=180.0)
     ap.add_argument("--list-workloads", action="store_true",
                     help="print each workload's configuration as one JSON line and exit")
     args = ap.parse_args()

@@ -304,6 +304,36 @@ extern "C" int fp8z1_copy_lut(const fp8z1_layout* L, fp8z1_block* host_dst, int6
     return FP8Z1_OK;
 }
 
+// §总结 ends by unfolding the 1-D blockwise scales into each param's 2-D / 3-D
+// scales.  Blocks run param by param and, inside a param, in (e, rb, cb)
+// row-major order (§参数布局变换), so a param's scales are one contiguous
+// [E, ceil(R/128), ceil(C/128)] stretch of the scale buffer; this reports
+// where it starts and which experts of it a block range holds whole.
+extern "C" int fp8z1_param_blocks(const fp8z1_layout* L, int32_t param, int64_t b0, int64_t b1,
+                                  fp8z1_param_grid* out)
+{
+    if (!L || !out || param < 0 || param >= L->n_params) return FP8Z1_EINVAL;
+    if (b0 < 0 || b1 < b0 || b1 > L->n_blocks) return FP8Z1_EINVAL;
+    const fp8z1_shape& sh = L->shapes[(size_t)param];
+    fp8z1_param_grid g;
+    g.first_block = L->param_block0[(size_t)param];
+    g.experts = sh.E;
+    g.row_blocks = tiles(sh.R);
+    g.col_blocks = tiles(sh.C);
+    const int64_t per = g.row_blocks * g.col_blocks;  // blocks of one expert
+    // experts e with [first + e*per, first + (e+1)*per) inside [b0, b1)
+    int64_t lo = b0 - g.first_block, hi = b1 - g.first_block;
+    int64_t e0 = lo <= 0 ? 0 : (lo + per - 1) / per;
+    int64_t e1 = hi <= 0 ? 0 : hi / per;
+    if (e0 > g.experts) e0 = g.experts;
+    if (e1 > g.experts) e1 = g.experts;
+    if (e1 < e0) e1 = e0;
+    g.e_begin = e0;
+    g.e_end = e1;
+    *out = g;
+    return FP8Z1_OK;
+}
+
 extern "C" int fp8z1_device_status(const fp8z1_layout* L, uint32_t* bits)
 {
     if (!L || !bits) return FP8Z1_EINVAL;

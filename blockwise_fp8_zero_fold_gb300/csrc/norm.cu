@@ -137,7 +137,8 @@ __device__ __forceinline__ void sum_unit(const float4 (&x)[kVec], double& acc, i
 // squares needs no block structure, so only partial strips need the table.
 // Each of these is two units: its first and second 8192 values (for a block
 // of the row-major params, its rows 0-63 and 64-127).
-enum Src { kFolded, kRows, kParams, kSpan };
+// A flat range of grads (an MXFP8 shard) is read the same way, run by run.
+enum Src { kFolded, kRows, kParams, kSpan, kFlat };
 
 // Where unit k's grads live in the row-major params.
 struct RowSrc {
@@ -229,20 +230,34 @@ __device__ __forceinline__ RowSrc span_src(const float* const* __restrict__ para
     return s;
 }
 
+// Run k of a flat range of `elems` grads at `base` (16-byte aligned):
+// elements 16384 k .. , the last run possibly short.
+__device__ __forceinline__ RowSrc flat_src(const float* base, int64_t elems, int64_t k)
+{
+    RowSrc s = {};
+    const int64_t o = k * FP8Z1_BLOCK_ELEMS;
+#if FP8Z1_CHECKED
+    s.first = o;
+    s.elems = elems;
+#endif
+    s.tile = base + o;
+    s.count = (int)(elems - o < FP8Z1_BLOCK_ELEMS ? elems - o : FP8Z1_BLOCK_ELEMS);
+    s.vec = true;
+    return s;
+}
+
 struct NormArgs {
-    const float4* g;              // folded grads at block b0 (kFolded)
+    const float4* g;              // folded grads at block b0 (kFolded); the flat grads (kFlat)
     const fp8z1_block* lut;       // kRows
     const fp8z1_unit* units;      // kParams
     const float* const* params;   // kRows, kParams, kSpan: row-major FP32 grads
     const int64_t* param_elems;   // kRows, kParams, kSpan: each param's extent (checked builds test against it)
     int64_t span_offset;          // kSpan: first element of the span in its param ...
-    int64_t span_elems;           // ... its length ...
+    int64_t span_elems;           // ... its length ... (kFlat: the flat range's length)
     int32_t span_param;           // ... and the param
     float4* store;                // STORE: folded grads at block b0
     int64_t b0;                   // first block (kRows: LUT index) or run (kParams)
     int64_t nblocks;              // blocks of 16384, the last one possibly partial (2 units each)
-    int64_t tail_k;               // kFolded: index of a partial last block ...
-    int tail_vec4;                // ... and its float4 count (0: no partial block)
     double* partials;             // one per CTA
     unsigned* counter;
     unsigned* status;
@@ -261,15 +276,10 @@ __device__ __forceinline__ void load_unit(const NormArgs& a, const RowSrc& s, in
 {
     const int h = (int)(u % kUnitsPerBlock);
     if constexpr (SRC == kFolded) {
-        // float4s of this unit that exist: all of them, except in a flat
-        // range's partial last block
-        int lim = kUnitElems / 4;
-        if (a.tail_vec4 != 0 && u / kUnitsPerBlock == a.tail_k) lim = a.tail_vec4 - h * (kUnitElems / 4);
         const float4* p = a.g + u * (kUnitElems / 4) + tid;
 #pragma unroll
-        for (int j = 0; j < kVec; ++j)
-            x[j] = tid + j * kThreads < lim ? __ldcs(p + j * kThreads) : make_float4(0.f, 0.f, 0.f, 0.f);
-    } else if constexpr (SRC == kParams || SRC == kSpan) {
+        for (int j = 0; j < kVec; ++j) x[j] = __ldcs(p + j * kThreads);
+    } else if constexpr (SRC == kParams || SRC == kSpan || SRC == kFlat) {
         const int e0 = h * kUnitElems;
         if (s.vec && s.count == FP8Z1_BLOCK_ELEMS) {  // a whole, aligned run
             const float4* p = reinterpret_cast<const float4*>(s.tile + e0) + tid;
@@ -339,6 +349,7 @@ __device__ __forceinline__ RowSrc src_of(const NormArgs& a, int64_t u)
     if (SRC == kRows) return row_src(a.lut, a.params, a.param_elems, a.b0 + k);
     if (SRC == kParams) return param_src(a.units, a.params, a.param_elems, a.b0 + k);
     if (SRC == kSpan) return span_src(a.params, a.param_elems, a.span_param, a.span_offset, a.span_elems, k);
+    if (SRC == kFlat) return flat_src(reinterpret_cast<const float*>(a.g), a.span_elems, k);
     return RowSrc{};
 }
 
@@ -561,8 +572,8 @@ extern "C" int fp8z1_fold_norm(const fp8z1_layout* L, const float* const* d_grad
 }
 
 // The grad norm of an MXFP8 shard: a flat range of (g1 - g0) groups of 32
-// FP32 grads, in the same reduction (its last 16384-element block may be
-// partial).
+// FP32 grads, in the same reduction, read as runs of 16384 (the last one
+// possibly short) the way whole params are read.
 extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_shard, int64_t g0,
                                   int64_t g1, double* d_sumsq, int32_t* d_found_inf, void* stream)
 {
@@ -576,17 +587,15 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
     if (n == 0) return FP8Z1_OK;
     NormArgs a = {};
     a.g = reinterpret_cast<const float4*>(grad_shard);
-    const int64_t full = n / FP8Z1_BLOCK_ELEMS, rem = n % FP8Z1_BLOCK_ELEMS;
-    a.nblocks = full + (rem ? 1 : 0);
-    a.tail_k = full;
-    a.tail_vec4 = (int)(rem / 4);
+    a.span_elems = n;
+    a.nblocks = (n + FP8Z1_BLOCK_ELEMS - 1) / FP8Z1_BLOCK_ELEMS;
     a.partials = L->d_partials;
     a.counter = L->d_counter;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
     fp8z1::count_launch();
-    norm_kernel<kFolded, false><<<(unsigned)persistent_grid(L, a.nblocks), kThreads, 0,
-                                 static_cast<cudaStream_t>(stream)>>>(a);
+    norm_kernel<kFlat, false><<<(unsigned)persistent_grid(L, a.nblocks), kThreads, 0,
+                               static_cast<cudaStream_t>(stream)>>>(a);
     return fp8z1::launch_status();
 }
 
@@ -602,24 +611,66 @@ extern "C" int fp8z1_mx_grad_norm(const fp8z1_mx_layout* L, const float* grad_sh
 //
 // Workspace: one double per CTA plus the finished-CTA counter, in a static
 // array that every device which loads the library holds until the process
-// exits (8 * (4096 + 1) bytes).  Each CTA covers up to 64 blocks, so one call
-// covers at most 4096 * 64 = 262144 blocks; larger ranges are rejected (split
-// them into several calls, which accumulate into the same *d_sumsq).
+// exits (8 * (4096 + 1) bytes).  A call runs the persistent grid of the other
+// entry points -- three CTAs per SM, at most one per half block -- so it
+// needs one slot per CTA: 4096 slots cover any device with up to 1365 SMs.
+// One call covers at most FP8Z1_NOALLOC_MAX_BLOCKS blocks (the header's
+// stated bound); larger ranges are rejected -- split them into several
+// calls, which accumulate into the same *d_sumsq.
 namespace {
 
-constexpr int64_t kNoAllocBlocksPerCta = 64;
-constexpr int kNoAllocMaxCtas = (int)(FP8Z1_NOALLOC_MAX_BLOCKS / kNoAllocBlocksPerCta);
+constexpr int kNoAllocMaxCtas = 4096;
 constexpr int kMaxDevices = 64;
 
 // partials[0, kNoAllocMaxCtas), then the counter (as an unsigned) in the last slot
 static __device__ __align__(256) double g_noalloc_scratch[kNoAllocMaxCtas + 1];
 
-std::mutex g_noalloc_mutex;
-double* g_noalloc_addr[kMaxDevices] = {};
+// What a device's first call looked up: the workspace's device address, the
+// device's SM count, and the CUDA context both belong to (by its unique id).
+// A device reset destroys the context and may load the module at another
+// address, so a new context id triggers a fresh lookup.
+struct NoAllocDevice {
+    double* addr = nullptr;
+    int sm_count = 0;
+    unsigned long long ctx_id = 0;
+};
 
-// The device address of the static workspace on the current device, looked up
-// once per device (host code cannot use the array's name as an address).
-int noalloc_workspace(double** out)
+std::mutex g_noalloc_mutex;
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+
+// The current context's unique id, through the driver's entry points (the
+// library does not link the driver library itself).  0 when it cannot be read.
+unsigned long long current_context_id()
+{
+    using GetCurrent = int (*)(void**);
+    using GetId = int (*)(void*, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(f);
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return 0;
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != 0 || ctx == nullptr || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+// The device address of the static workspace on the current device and the
+// device's SM count, looked up on the host with that device current (host
+// code cannot use the array's name as an address): once per device, and
+// again only when the device's context has changed.
+int noalloc_workspace(double** out, int* sm_count)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -627,16 +678,25 @@ int noalloc_workspace(double** out)
         return FP8Z1_ECUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return FP8Z1_ECUDA;
+    // 0 before the device's context exists: the lookup below creates it
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_addr[dev] == nullptr) {
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (d.addr == nullptr || ctx == 0 || ctx != d.ctx_id) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        int sms = 0;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
             cudaGetLastError();
+            d = NoAllocDevice();
             return FP8Z1_ECUDA;
         }
-        g_noalloc_addr[dev] = static_cast<double*>(p);
+        d.addr = static_cast<double*>(p);
+        d.sm_count = sms;
+        d.ctx_id = current_context_id();
     }
-    *out = g_noalloc_addr[dev];
+    *out = d.addr;
+    *sm_count = d.sm_count;
     return FP8Z1_OK;
 }
 
@@ -645,13 +705,15 @@ int noalloc_workspace(double** out)
 extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks, double* d_sumsq,
                                        int32_t* d_found_inf, void* stream)
 {
+    fp8z1::NvtxRange nvtx_range("fp8z1_grad_norm_noalloc");
     if (!grad_shard || !d_sumsq || !d_found_inf || n_blocks < 0) return FP8Z1_EINVAL;
-    if (n_blocks > FP8Z1_NOALLOC_MAX_BLOCKS) return FP8Z1_EINVAL;  // beyond the static workspace
+    if (n_blocks > FP8Z1_NOALLOC_MAX_BLOCKS) return FP8Z1_EINVAL;  // beyond the stated bound
     if (!fp8z1::aligned(grad_shard, 16) || !fp8z1::aligned(d_sumsq, 8) || !fp8z1::aligned(d_found_inf, 4))
         return FP8Z1_EALIGN;
     if (n_blocks == 0) return FP8Z1_OK;
     double* partials = nullptr;
-    const int st = noalloc_workspace(&partials);
+    int sm_count = 0;
+    const int st = noalloc_workspace(&partials, &sm_count);
     if (st != FP8Z1_OK) return st;
     unsigned* counter = reinterpret_cast<unsigned*>(partials + kNoAllocMaxCtas);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -667,7 +729,9 @@ extern "C" int fp8z1_grad_norm_noalloc(const float* grad_shard, int64_t n_blocks
     a.counter = counter;
     a.sumsq = d_sumsq;
     a.found_inf = d_found_inf;
-    const int64_t grid = (n_blocks + kNoAllocBlocksPerCta - 1) / kNoAllocBlocksPerCta;
+    int64_t grid = (int64_t)sm_count * kCtasPerSm;
+    if (grid > n_blocks * kUnitsPerBlock) grid = n_blocks * kUnitsPerBlock;
+    if (grid > kNoAllocMaxCtas) grid = kNoAllocMaxCtas;
     fp8z1::count_launch();
     norm_kernel<kFolded, false><<<(unsigned)grid, kThreads, 0, s>>>(a);
     return fp8z1::launch_status();

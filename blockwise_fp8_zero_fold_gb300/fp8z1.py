@@ -53,6 +53,11 @@ class fp8z1_block(C.Structure):
                 ("rows_real", C.c_int16), ("cols_real", C.c_int16)]
 
 
+class fp8z1_param_grid(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("first_block", "experts", "row_blocks", "col_blocks",
+                                          "e_begin", "e_end")]
+
+
 class fp8z1_adamw_hp(C.Structure):
     _fields_ = [("lr", C.c_float), ("beta1", C.c_float), ("beta2", C.c_float),
                 ("eps", C.c_float), ("weight_decay", C.c_float), ("max_norm", C.c_float),
@@ -84,6 +89,7 @@ _SIGS = {
                                     C.POINTER(C.c_int64)]),
     "fp8z1_shard_range": (C.c_int, [_P, C.c_int32, C.POINTER(C.c_int64), C.POINTER(C.c_int64)]),
     "fp8z1_copy_lut": (C.c_int, [_P, _P, C.c_int64]),
+    "fp8z1_param_blocks": (C.c_int, [_P, C.c_int32, C.c_int64, C.c_int64, C.POINTER(fp8z1_param_grid)]),
     "fp8z1_device_status": (C.c_int, [_P, C.POINTER(C.c_uint32)]),
     "fp8z1_fold": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int64, C.c_int64, _P]),
     "fp8z1_unfold": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int64, C.c_int64, _P]),
@@ -231,6 +237,15 @@ def fp8z1_copy_lut(layout: Layout) -> np.ndarray:
     out = np.zeros(max(1, nblk), dtype=BLOCK_DTYPE)
     _check(lib().fp8z1_copy_lut(layout.handle, out.ctypes.data, nblk), "fp8z1_copy_lut")
     return out[:nblk]
+
+
+def fp8z1_param_blocks(layout: Layout, param: int, b0: int, b1: int) -> fp8z1_param_grid:
+    """Where param ``param``'s blocks (and so its scales) sit in the flat
+    block order, and the experts whose blocks all lie in [b0, b1)."""
+    g = fp8z1_param_grid()
+    _check(lib().fp8z1_param_blocks(layout.handle, int(param), int(b0), int(b1), C.byref(g)),
+           "fp8z1_param_blocks")
+    return g
 
 
 def fp8z1_device_status(layout: Layout) -> int:

@@ -38,6 +38,20 @@ import torch
 from . import fp8z1 as F
 
 
+def shard_scale_view(layout, scales: torch.Tensor, b0: int, b1: int, param: int):
+    """``(e0, view)`` over the experts of ``param`` whose blocks all lie in the
+    shard [b0, b1), where ``scales`` holds the shard's b1 - b0 block scales
+    (block b0 first); None when there are none.  The block order is the
+    layout's (fp8z1_param_blocks): the view is a slice of ``scales``."""
+    g = F.fp8z1_param_blocks(layout, param, b0, b1)
+    if g.e_end <= g.e_begin:
+        return None
+    per = g.row_blocks * g.col_blocks
+    lo = g.first_block + g.e_begin * per - b0
+    n = g.e_end - g.e_begin
+    return g.e_begin, scales[lo:lo + n * per].view(n, g.row_blocks, g.col_blocks)
+
+
 class _AsyncSteps:
     """Steps enqueued ahead of their found_inf, shared by both optimizers.
 
@@ -225,15 +239,24 @@ class ShardOptimizer(_AsyncSteps):
         if v is not None:
             self.fold_into(v, self.v, stream)
 
-    def scale_views(self) -> List[torch.Tensor]:
-        """Per-param [E, ceil(R/128), ceil(C/128)] views of the scale buffer
-        (whole-buffer shards only)."""
-        assert self.b0 == 0 and self.b1 == self.nblk
-        out, off = [], 0
-        for e, r, c in self.shapes:
-            rb, cb = -(-r // 128), -(-c // 128)
-            out.append(self.scales[off:off + e * rb * cb].view(e, rb, cb))
-            off += e * rb * cb
+    def scale_view(self, param: int):
+        """The scales of param ``param``'s experts that this shard holds whole,
+        as ``(e0, view)``: ``view[e - e0, rb, cb]`` is the scale of block
+        (e, rb, cb) of the param, a [n, ceil(R/128), ceil(C/128)] view of the
+        scale buffer (no copy).  None when the shard holds no whole expert of
+        the param.  Where the blocks sit comes from the layout
+        (fp8z1_param_blocks)."""
+        return shard_scale_view(self.layout, self.scales, self.b0, self.b1, param)
+
+    def scale_views(self) -> List[Optional[torch.Tensor]]:
+        """Per param, its [E, ceil(R/128), ceil(C/128)] scale tensor as a view
+        of the scale buffer when this shard holds the whole param, else None
+        ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结: the 1-D blockwise
+        scales unfolded back into 2-D / 3-D scales)."""
+        out = []
+        for p, shp in enumerate(self.shapes):
+            v = self.scale_view(p)
+            out.append(v[1] if v is not None and v[0] == 0 and v[1].shape[0] == shp[0] else None)
         return out
 
     # -- checkpoint / resume --------------------------------------------------

@@ -16,6 +16,8 @@ Workloads (each tensor is a row-major float32 [E, R, C]; 2-D weights have E=1):
 * ``ragged`` 4000 2-D tensors, R and C uniform in [17, 690] and never a
              multiple of 128; loss scale 65536, max_norm 0.8; +inf written
              into element (0, 0) of tensor 1234 on step 2.
+* ``ragged_literal`` the same with R and C uniform in [17, 3000] (9.08 G
+             real elements, 602268 blocks, about 160 GB on the device).
 * ``large``  64 experts of 7168x4096 and 2048x7168 plus dense 7168x18432
              tensors (x9 for the 4.0 G-element reading, x4 for the literal list).
 
@@ -95,8 +97,9 @@ def workload(name: str, **overrides) -> Workload:
     elif name == "moe":
         w = Workload("moe", [(32, 7168, 4096), (32, 2048, 7168)], dp=8, rank=3, steps=5,
                      grad_sigma=1e-4, m_sigma=1e-4, v_sigma=1e-8, zero_tile_frac=0.01)
-    elif name == "ragged":
-        w = Workload("ragged", ragged_shapes(), dp=1, rank=0, steps=3, grad_sigma=1e-3,
+    elif name in ("ragged", "ragged_literal"):
+        hi = 690 if name == "ragged" else 3000
+        w = Workload(name, ragged_shapes(hi=hi), dp=1, rank=0, steps=3, grad_sigma=1e-3,
                      loss_scale=65536.0, max_norm=0.8, inf_step=2, inf_param=1234)
     elif name in ("large", "large_literal"):
         dense = 9 if name == "large" else 4

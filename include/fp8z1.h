@@ -136,6 +136,30 @@ int fp8z1_shard_range(const fp8z1_layout* layout, int32_t rank, int64_t* b0, int
  * of entries `host_dst` holds (EINVAL when too small). */
 int fp8z1_copy_lut(const fp8z1_layout* layout, fp8z1_block* host_dst, int64_t capacity);
 
+/* Where one param's blocks sit in the flat block order, and so where its
+ * scales sit in the scale buffer (§总结: the 1-D blockwise scales unfolded
+ * back into each param's 2-D / 3-D scales).  Block (e, rb, cb) of the param
+ * is global block first_block + (e * row_blocks + rb) * col_blocks + cb, so
+ * scales[first_block .. + experts * row_blocks * col_blocks) is the param's
+ * [E, ceil(R/128), ceil(C/128)] scale tensor, row-major, with no copy. */
+typedef struct {
+    int64_t first_block; /* global index of block (0, 0, 0) of the param */
+    int64_t experts;     /* E */
+    int64_t row_blocks;  /* ceil(R / 128) */
+    int64_t col_blocks;  /* ceil(C / 128) */
+    int64_t e_begin;     /* experts [e_begin, e_end) have every block inside */
+    int64_t e_end;       /* the range [b0, b1) asked about; equal when none */
+} fp8z1_param_grid;
+
+/* Fill *out for param `param` (0 <= param < n_params) and the block range
+ * [b0, b1) (0 <= b0 <= b1 <= n_blocks), e.g. a rank's shard: a shard's scale
+ * buffer, which starts at block b0, then holds experts [e_begin, e_end) of
+ * the param as the [e_end - e_begin, row_blocks, col_blocks] stretch at
+ * first_block + e_begin * row_blocks * col_blocks - b0.  Host only; works on
+ * host-only layouts.  Errors: EINVAL (null, param or range out of bounds). */
+int fp8z1_param_blocks(const fp8z1_layout* layout, int32_t param, int64_t b0, int64_t b1,
+                       fp8z1_param_grid* out);
+
 /* Read and clear the layout's device status word (synchronous; waits for the
  * copy).  Bit 1 (FP8Z1_DEVSTATUS_BADPTR): a fold, unfold, fused norm or
  * fused step met a param pointer in its device pointer array that was null or
@@ -200,12 +224,17 @@ int fp8z1_norm_reset(double* d_sumsq, int32_t* d_found_inf, void* stream);
  * summation is split differently, so the two results agree to about 1e-13
  * relative, not bit for bit.  It needs no layout and allocates nothing: its
  * workspace is a static device array of 4097 doubles (about 32 KB) that every
- * device loading the library holds until the process exits.
+ * device loading the library holds until the process exits.  It runs the
+ * same persistent grid as fp8z1_grad_norm (three CTAs per SM, at most one
+ * per half block), one workspace slot per CTA.
  *   - At most FP8Z1_NOALLOC_MAX_BLOCKS blocks per call (EINVAL beyond that);
  *     split a larger range into several calls, which accumulate.
- *   - The first call on each device looks up the workspace address on the
- *     host (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture.
+ *   - The first call on each device looks up the workspace address and the
+ *     SM count on the host (cudaGetSymbolAddress, with that device current);
+ *     make that first call before any stream capture.  The lookup is tied
+ *     to the device's CUDA context: after a device reset (cudaDeviceReset)
+ *     the next call looks the address up again, so it too must come before
+ *     any capture.
  *   - Every call shares the one workspace, and a call leaves its contents
  *     behind; the call clears the part that must start at zero on its
  *     stream.  Calls that overlap on the device race: issue them on one

@@ -45,7 +45,8 @@ def test_list_workloads():
     assert r.returncode == 0, r.stderr[-2000:]
     got = {d["name"]: d for d in map(json.loads, r.stdout.splitlines())}
     assert {k: v["n_blocks"] for k, v in got.items()} == {
-        "tiny": 6, "dense": 15040, "moe": 86016, "ragged": 42706, "large": 244608, "large_literal": 204288}
+        "tiny": 6, "dense": 15040, "moe": 86016, "ragged": 42706, "ragged_literal": 602268, "large": 244608,
+        "large_literal": 204288}
     assert got["moe"]["n_real"] == 1409286144 and (got["moe"]["dp"], got["moe"]["rank"]) == (8, 3)
     assert got["ragged"]["n_params"] == 4000 and got["ragged"]["inf_step"] == 2
 
@@ -67,8 +68,15 @@ def _check_ours(d, steps):
 @pytest.mark.gpu
 def test_bench_line_tiny():
     d = _run("--workload", "tiny", "--steps", "4", "--warmup", "3", "--compare", "1", "--e2e-steps", "2",
-             "--cpu-sample-experts", "1", "--monitors", "2")
+             "--cpu-sample-experts", "1", "--monitors", "2", "--other-workloads", "tiny,tiny@2:1",
+             "--other-steps", "3")
     _check_ours(d, 4)
+    ow = d["other_workloads"]
+    assert [o["blocks"] for o in ow] == [6, 3] and ow[1]["dp"].startswith("rank 1 of 2")
+    for o in ow:
+        assert o["steps"] == 3 and o["ms_per_step"] > 0 and o["skipped_steps"] == 0
+        assert set(o["kernels_ms"]) == set(o["kernels_gbs"]) == set(o["frac_of_measured"]) == {"fold_norm", "step"}
+        assert o["kernels_gbs"]["step"] == pytest.approx(o["bytes_per_launch"]["step"] / o["kernels_ms"]["step"] / 1e6)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
     assert len(e["ms_per_step_reps"]) == len(e["ms_per_step_one_at_a_time_reps"]) == e["reps"] == 3
@@ -87,7 +95,7 @@ def test_bench_line_tiny():
 @pytest.mark.gpu
 def test_bench_line_shard_and_bf16_fold():
     d = _run("--workload", "dense", "--shard", "4:1", "--steps", "3", "--warmup", "3", "--compare", "0",
-             "--e2e-steps", "0", "--cpu-sample-experts", "0", "--bf16-fold", "2")
+             "--e2e-steps", "0", "--cpu-sample-experts", "0", "--bf16-fold", "2", "--other-workloads", "")
     _check_ours(d, 3)
     assert d["config"]["dp"].startswith("rank 1 of 4")
     assert d["config"]["blocks"] == 3760 and d["e2e"] is None

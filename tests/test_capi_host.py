@@ -112,6 +112,57 @@ def test_host_lut_bit_exact_against_oracle(shapes):
         assert F.fp8z1_shard_range(L, r) == oracle.shard_range(nblk, 3, r)
 
 
+@pytest.mark.parametrize("shapes", LUT_CASES, ids=lambda s: str(len(s)))
+def test_param_blocks_against_oracle_lut(shapes):
+    """fp8z1_param_blocks (where a param's blocks, and so its scales, sit):
+    for every param and several ranges, checked against the oracle's block
+    table by brute force -- the first block is the first the table gives the
+    param, every (e, rb, cb) sits at first + (e*Rb + rb)*Cb + cb, and the
+    experts reported held are exactly those whose every block lies in the
+    range ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结, §参数布局变换)."""
+    from blockwise_fp8_zero_fold_gb300.optimizer import shard_scale_view
+    import torch
+    ref = oracle.build_lut(shapes)
+    nblk = len(ref)
+    ranges = [(0, nblk), (0, 0), (nblk, nblk)]
+    for dp in (2, 3, 8):
+        ranges += [oracle.shard_range(nblk, dp, r) for r in range(dp)]
+    rng = np.random.default_rng(len(shapes))
+    for _ in range(6):
+        a, b = sorted(int(x) for x in rng.integers(0, nblk + 1, 2))
+        ranges.append((a, b))
+    L = F.fp8z1_build_layout(shapes, host_only=True)
+    scales = torch.arange(nblk, dtype=torch.float64)  # scale k holds k
+    for p in range(len(shapes)):
+        mine = np.flatnonzero(ref[:, 0] == p)
+        E = int(ref[mine, 1].max()) + 1
+        Rb = int(ref[mine, 2].max()) + 1
+        Cb = int(ref[mine, 3].max()) + 1
+        for b0, b1 in ranges:
+            g = F.fp8z1_param_blocks(L, p, b0, b1)
+            assert (g.first_block, g.experts, g.row_blocks, g.col_blocks) == (mine[0], E, Rb, Cb)
+            where = g.first_block + (ref[mine, 1] * Rb + ref[mine, 2]) * Cb + ref[mine, 3]
+            assert np.array_equal(where, mine)
+            held = [e for e in range(E)
+                    if all(b0 <= k < b1 for k in mine[ref[mine, 1] == e])]
+            want = (held[0], held[-1] + 1) if held else None
+            got = (g.e_begin, g.e_end) if g.e_end > g.e_begin else None
+            assert got == want, (p, b0, b1)
+            v = shard_scale_view(L, scales[b0:b1], b0, b1, p)
+            if want is None:
+                assert v is None
+                continue
+            e0, view = v
+            assert e0 == want[0] and tuple(view.shape) == (want[1] - want[0], Rb, Cb)
+            for k in mine[(ref[mine, 1] >= want[0]) & (ref[mine, 1] < want[1])][:50]:
+                e, rb, cb = (int(x) for x in ref[k, 1:4])
+                assert view[e - e0, rb, cb].item() == k
+    with pytest.raises(F.Fp8z1Error):
+        F.fp8z1_param_blocks(L, len(shapes), 0, nblk)
+    with pytest.raises(F.Fp8z1Error):
+        F.fp8z1_param_blocks(L, 0, 0, nblk + 1)
+
+
 @pytest.mark.parametrize("row", rows("layout_counts.txt"), ids=lambda r: f"{r[0]}-r{r[4]}")
 def test_golden_counts_and_ranges_through_abi(row):
     name, shapes, nblk, dp, rank, b0, b1 = row

@@ -21,6 +21,7 @@ import torch
 import oracle
 from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
 from blockwise_fp8_zero_fold_gb300 import synth
+from blockwise_fp8_zero_fold_gb300.optimizer import shard_scale_view
 from tests._gpu import assert_codes, assert_rel, lib, to_host  # noqa: F401
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +51,7 @@ class Harness:
         self.fp8_ptrs = F.param_pointers(self.fp8)
         self.scaler = F.fp8z1_loss_scaler(w.loss_scale, 0, 0, w.growth_interval)
         self.oscaler = oracle.Scaler(w.loss_scale, w.growth_interval)
+        self.views_checked = 0
 
         rng = np.random.default_rng(1234 + rank)
         pick = set(int(x) for x in rng.choice(np.arange(self.b0, self.b1), min(n_sample, nb), replace=False))
@@ -80,6 +82,28 @@ class Harness:
     def oracle_block(self, rm, k):
         t = np.ascontiguousarray(to_host(self.tile(rm, k)))
         return oracle.fold([(1,) + t.shape], [t.reshape((1,) + t.shape)])
+
+    def check_scale_views(self, want):
+        """The per-param scale views (the scales "unfolded" to [E, R/128,
+        C/128], §总结) hold, at the (p, e, rb, cb) the oracle's table gives
+        each sampled block, the oracle's scale of that block; a param with no
+        expert wholly in the shard has no view."""
+        views, wholes = {}, {}
+        for i, k in enumerate(self.sample):
+            p, e, rb, cb = (int(x) for x in self.lut[k][:4])
+            if p not in views:
+                views[p] = shard_scale_view(self.L, self.scales, self.b0, self.b1, p)
+                mine = np.flatnonzero(self.lut[:, 0] == p)
+                ex = self.lut[mine, 1]
+                wholes[p] = {ee for ee in range(int(ex.max()) + 1)
+                             if ((mine[ex == ee] >= self.b0) & (mine[ex == ee] < self.b1)).all()}
+            v = views[p]
+            if e not in wholes[p]:
+                assert v is None or not (v[0] <= e < v[0] + v[1].shape[0])
+                continue
+            e0, view = v
+            assert float(view[e - e0, rb, cb]) == float(want[i]), (k, p, e, rb, cb)
+            self.views_checked += 1
 
     def gather(self, buf, per_block=B):
         return to_host(buf.view(-1, per_block)[self.local]) if per_block > 1 else to_host(buf[self.local])
@@ -134,6 +158,7 @@ class Harness:
         if not f_exact:
             gs = self.gather(self.scales, per_block=1)
             assert_rel(gs, s, 1e-6, "scales")
+            self.check_scale_views(s)
             gq = self.gather(self.codes)
             frac = assert_codes(gq, q, "codes")
             exact = exact and frac == 0.0 and np.array_equal(gs, s)
@@ -163,12 +188,20 @@ def test_tiny_all_blocks(lib, rank):
     h, out = _run(w, rank, w.steps, n_sample=10)
     assert len(h.sample) == 3 and [f for f, _ in out] == [0, 0, 0]
     assert all(e for _, e in out)
+    assert h.views_checked == 0  # each rank holds half of the one weight: no view
 
 
 def test_dense_ten_steps(lib):
     w = synth.workload("dense")
     h, out = _run(w, 0, w.steps, n_sample=160)
     assert all(f == 0 for f, _ in out) and all(e for _, e in out)
+    assert h.views_checked == len(h.sample) * w.steps
+
+
+def test_tiny_whole_weight_scale_view(lib):
+    w = synth.workload("tiny", dp=1, rank=0)
+    h, out = _run(w, 0, w.steps, n_sample=10)
+    assert len(h.sample) == 6 and h.views_checked == 6 * w.steps
 
 
 def test_moe_rank3_of_8(lib):
@@ -176,6 +209,11 @@ def test_moe_rank3_of_8(lib):
     h, out = _run(w, 3, w.steps, n_sample=160)
     assert (h.b0, h.b1) == (32256, 43008)
     assert all(f == 0 for f, _ in out) and all(e for _, e in out)
+    # the shard holds experts 18-23 of gate_up whole: their scale view
+    assert h.views_checked == len(h.sample) * w.steps
+    e0, view = shard_scale_view(h.L, h.scales, h.b0, h.b1, 0)
+    assert e0 == 18 and tuple(view.shape) == (6, 56, 32)
+    assert shard_scale_view(h.L, h.scales, h.b0, h.b1, 1) is None
 
 
 def test_moe_full_buffer_with_zero_blocks(lib):
@@ -202,6 +240,7 @@ def test_ragged_skip_step(lib):
     h, out = _run(w, 0, w.steps, n_sample=240, must=must)
     assert [f for f, _ in out] == [0, 1, 0]
     assert all(e for _, e in out)
+    assert h.views_checked == len(h.sample) * 2  # the two steps not skipped
     # S halves on the skipped step and t does not advance
     assert (h.scaler.scale, h.scaler.step) == (32768.0, 2)
 
@@ -276,6 +315,9 @@ def test_bench_loop_every_block(lib, name):
 
     exact, fi = oracle.sumsq_parallel([to_host(g) for g in grads], threads=16)
     assert fi == 0 and abs(float(opt.sumsq.item()) - exact) <= 1e-12 * exact
+    views = opt.scale_views()  # the whole buffer: every param has its view
+    assert all(v is not None and tuple(v.shape) == (e, -(-r // 128), -(-c // 128))
+               for v, (e, r, c) in zip(views, w.shapes))
     for i, k in enumerate(sample):
         g = oblock(grads, k)
         for t in range(1, 4):
@@ -286,6 +328,7 @@ def test_bench_loop_every_block(lib, name):
             assert np.array_equal(got.view(np.uint32), state[name][i].view(np.uint32)), (name, k)
         assert float(opt.scales[k]) == float(sc[0])
         p, e, rb, cb, rr, cr = (int(x) for x in lut[k])
+        assert float(views[p][e, rb, cb]) == float(sc[0]), k
         want = np.zeros((1, rr, cr), np.uint8)
         oracle.unfold([(1, rr, cr)], q, [want])
         assert np.array_equal(to_host(tile(fp8, k)), want[0]), k
