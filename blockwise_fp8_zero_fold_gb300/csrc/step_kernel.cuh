@@ -34,8 +34,16 @@
 // in grad, master, m and v (fold writes them so), and the update maps them to
 // zero again (g = 0 gives m = v = +0 and p = fma(-a, +0, +0) = +0), so a block
 // that is not a full 128x128 tile skips the float4 chunks that hold padding
-// only: no load, no store, new master 0 (which leaves the amax alone), code
-// 0x00 in the folded code shard.  Full tiles take the loop without the test.
+// only: no load, no store, new master 0 (which leaves the amax alone), and no
+// code to compute -- 0x00 goes to a folded code shard, nothing to the
+// row-major params.  (Computing those codes anyway, four divisions a chunk,
+// cost the ragged workload's step 4-5%.)  Full tiles take the loops without
+// the test.
+//
+// Row-major grads and codes of a param whose C is not a multiple of 4 start
+// each row at a different alignment; a chunk there is read and written with
+// the widest access its address allows (16 or 8 bytes of grads, 4 or 2 of
+// codes), one element at a time only where it must be.
 #pragma once
 
 #include <math.h>
@@ -68,10 +76,23 @@ __device__ __forceinline__ float4 load_grad_rows(const float* tile, int64_t ld, 
         if (vec) {  // ld % 4 == 0: a 4-column group is all real or all padding
             if (c < cols && in_extent(at, 4, elems)) g = __ldcs(reinterpret_cast<const float4*>(src));
         } else {
-            if (c + 0 < cols && in_extent(at + 0, 1, elems)) g.x = __ldcs(src + 0);
-            if (c + 1 < cols && in_extent(at + 1, 1, elems)) g.y = __ldcs(src + 1);
-            if (c + 2 < cols && in_extent(at + 2, 1, elems)) g.z = __ldcs(src + 2);
-            if (c + 3 < cols && in_extent(at + 3, 1, elems)) g.w = __ldcs(src + 3);
+            // rows of a param whose C % 4 != 0 start at different alignments:
+            // the widest access this chunk's address allows, when it is all real
+            const uintptr_t ad = reinterpret_cast<uintptr_t>(src);
+            if (c + 3 < cols && (ad & 15) == 0) {
+                if (in_extent(at, 4, elems)) g = __ldcs(reinterpret_cast<const float4*>(src));
+            } else if (c + 3 < cols && (ad & 7) == 0) {
+                if (in_extent(at, 4, elems)) {
+                    const float2 lo = __ldcs(reinterpret_cast<const float2*>(src));
+                    const float2 hi = __ldcs(reinterpret_cast<const float2*>(src + 2));
+                    g = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+            } else {
+                if (c + 0 < cols && in_extent(at + 0, 1, elems)) g.x = __ldcs(src + 0);
+                if (c + 1 < cols && in_extent(at + 1, 1, elems)) g.y = __ldcs(src + 1);
+                if (c + 2 < cols && in_extent(at + 2, 1, elems)) g.z = __ldcs(src + 2);
+                if (c + 3 < cols && in_extent(at + 3, 1, elems)) g.w = __ldcs(src + 3);
+            }
         }
     }
     return g;
@@ -86,9 +107,19 @@ __device__ __forceinline__ void store_codes_rows(uint8_t* tile, int64_t ld, int 
     if (vec) {
         if (c < cols && in_extent(at, 4, elems)) __stcs(reinterpret_cast<unsigned int*>(dst), q);
     } else {
+        const uintptr_t ad = reinterpret_cast<uintptr_t>(dst);
+        if (c + 3 < cols && (ad & 3) == 0) {
+            if (in_extent(at, 4, elems)) __stcs(reinterpret_cast<unsigned int*>(dst), q);
+        } else if (c + 3 < cols && (ad & 1) == 0) {
+            if (in_extent(at, 4, elems)) {
+                __stcs(reinterpret_cast<unsigned short*>(dst), (unsigned short)(q & 0xffffu));
+                __stcs(reinterpret_cast<unsigned short*>(dst + 2), (unsigned short)(q >> 16));
+            }
+        } else {
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-            if (c + b < cols && in_extent(at + b, 1, elems)) dst[b] = (uint8_t)(q >> (8 * b));
+            for (int b = 0; b < 4; ++b)
+                if (c + b < cols && in_extent(at + b, 1, elems)) dst[b] = (uint8_t)(q >> (8 * b));
+        }
     }
 }
 
@@ -260,8 +291,19 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
 
     float pd = 0.0f, pp = 0.0f, dd = 0.0f;
     uint32_t under = 0u;
+    // chunks j >= jn hold padding only: their new masters are 0, their codes
+    // 0x00 (stored only into a folded code shard), their monitor terms 0
+    int jn = kVec;
+    if (PAD) {
+        const int row0 = tid >> 5, col = (tid & 31) << 2;
+        jn = col >= cols ? 0 : min(kVec, max(0, (rows - row0 + 15) >> 4));
+    }
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
+        if (PAD && j >= jn) {
+            if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, 0u);
+            continue;
+        }
         const float4 p = pn[j * kThreads];
         const uint32_t lo = e4m3x2(__fdiv_rn(p.x, scale), __fdiv_rn(p.y, scale));
         const uint32_t hi = e4m3x2(__fdiv_rn(p.z, scale), __fdiv_rn(p.w, scale));
