@@ -13,7 +13,11 @@
 // One CTA of 512 threads per block of 16384 elements, three CTAs per SM;
 // thread t owns the float4 chunks t, t+512, ..., t+3584 of the block (chunk i
 // is row i/32, columns 4*(i%32) .. +3 of the 128x128 block, so a warp covers
-// one block row).  It streams grad / master / m / v in, updates them, writes
+// one block row).  A partial block whose real columns fit in 64, 32, ... (W
+// float4 chunks a row, a power of two) has each warp cover 32 / W rows at a
+// time instead, so its warps finish in fewer passes (ragged's step 2.405 ->
+// 2.313 ms); the new master of chunk j of thread t still waits in shared-memory
+// slot t + 512 j.  It streams grad / master / m / v in, updates them, writes
 // master / m / v back at once and keeps its 32 new master values in its slots
 // of a 64 KB shared array while the CTA reduces the block amax (warp
 // shuffles, then 16 partials in shared memory).  The codes are then produced
@@ -152,31 +156,58 @@ constexpr int kMasterSmemBytes = kThreads * kVec * 16;
 // The update of this thread's 8 float4 chunks of the block: new masters into
 // pn[j * kThreads] (shared memory), their largest magnitude into amax.  PAD: skip the chunks that hold
 // padding only (chunk j of thread t is row t/32 + 16 j, columns 4 (t%32) .. +3).
+// Where this thread's chunks of a block sit.  A warp takes 32 / W rows at a
+// time, W = the block's real chunks a row rounded up to a power of two (sh =
+// log2(32 / W); sh = 0 for a block with more than 64 real columns and in
+// every full-tile launch): lane l has chunk l % W of row l / W of the warp's
+// rows, and chunk j of thread t is row rbase + j * (16 << sh), folded float4
+// index ibase + j * (512 << sh); jn of them hold real elements.
+struct ChunkPlace {
+    int64_t ibase;
+    int rbase, col, sh, jn;
+};
+
+template <bool PAD>
+__device__ __forceinline__ ChunkPlace chunk_place(int64_t kb, int tid, int rows, int cols, int sh)
+{
+    ChunkPlace c;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int rsub = lane >> (5 - sh), cc = lane & ((32 >> sh) - 1);
+    c.sh = sh;
+    c.rbase = (warp << sh) + rsub;
+    c.col = cc << 2;
+    c.ibase = kb * (FP8Z1_BLOCK_ELEMS / 4) + (int64_t)c.rbase * (FP8Z1_TILE / 4) + cc;
+    c.jn = kVec;
+    if (PAD) {
+        // tasks of 2^sh rows this lane has real rows in, then the chunks j < jn
+        const int tasks = rows > rsub ? (rows - rsub + (1 << sh) - 1) >> sh : 0;
+        c.jn = c.col >= cols ? 0 : min(kVec, max(0, (tasks - warp + 15) >> 4));
+    }
+    return c;
+}
+
 template <bool GRAD_ROWS, bool PAD>
-__device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, int64_t base,
-                                              int tid, const float* gtile, int64_t ld, int rows, int cols,
+__device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, const ChunkPlace& cp,
+                                              const float* gtile, int64_t ld, int rows, int cols,
                                               bool gvec, int64_t first, int64_t elems, float4* pn,
                                               float& amax)
 {
-    const int row0 = tid >> 5, col = (tid & 31) << 2;
-    // chunks j < jn hold real elements (rows grow with j, the column does not)
-    int jn = kVec;
-    if (PAD) jn = col >= cols ? 0 : min(kVec, max(0, (rows - row0 + 15) >> 4));
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-        if (PAD && j >= jn) {
+        if (PAD && j >= cp.jn) {
             pn[j * kThreads] = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
-        const int64_t i = base + j * kThreads;
+        const int64_t i = cp.ibase + ((int64_t)j * kThreads << (PAD ? cp.sh : 0));
+        const int row = cp.rbase + ((16 * j) << (PAD ? cp.sh : 0));
         float4 g4;
         if (GRAD_ROWS) {
             if (!PAD && gvec) {  // a full tile (every launch without PAD), 16-byte rows
-                const int64_t at = (int64_t)(row0 + 16 * j) * ld + col;
+                const int64_t at = (int64_t)row * ld + cp.col;
                 g4 = in_extent(first + at, 4, elems) ? __ldcs(reinterpret_cast<const float4*>(gtile + at))
                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
             } else {
-                g4 = load_grad_rows(gtile, ld, row0 + 16 * j, col, rows, cols, gvec, first, elems);
+                g4 = load_grad_rows(gtile, ld, row, cp.col, rows, cols, gvec, first, elems);
             }
         } else {
             g4 = __ldcs(a.grad + i);
@@ -263,6 +294,14 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
     const float gs = s_gscale;
 
     const int64_t base = kb * (FP8Z1_BLOCK_ELEMS / 4) + tid;
+    // narrow blocks take several rows a warp, except into a folded code shard
+    // (which wants every chunk of the block written)
+    int sh = 0;
+    if (PAD && !CODES_FOLDED) {
+        const int nc = (cols + 3) >> 2;
+        sh = nc > 16 ? 0 : nc > 8 ? 1 : nc > 4 ? 2 : nc > 2 ? 3 : nc > 1 ? 4 : 5;
+    }
+    const ChunkPlace cp = chunk_place<PAD>(kb, tid, rows, cols, sh);
     extern __shared__ float4 s_pn[];  // kMasterSmemBytes: the block's new masters
     float4* const pn = s_pn + tid;
     float amax = 0.0f;
@@ -270,13 +309,13 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
         // one uniform branch, each side with its scalars as kernel-parameter
         // operands (no registers held for them)
         if (s_alt)
-            update_chunks<GRAD_ROWS, PAD>(a, a.c2, gs, base, tid, gtile, ld, rows, cols, gvec, off, elems, pn,
+            update_chunks<GRAD_ROWS, PAD>(a, a.c2, gs, cp, gtile, ld, rows, cols, gvec, off, elems, pn,
                                           amax);
         else
-            update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, base, tid, gtile, ld, rows, cols, gvec, off, elems, pn,
+            update_chunks<GRAD_ROWS, PAD>(a, a.c, gs, cp, gtile, ld, rows, cols, gvec, off, elems, pn,
                                           amax);
     } else {
-        update_chunks<GRAD_ROWS, PAD>(a, kSmemScalars ? s_c : a.c, gs, base, tid, gtile, ld, rows, cols,
+        update_chunks<GRAD_ROWS, PAD>(a, kSmemScalars ? s_c : a.c, gs, cp, gtile, ld, rows, cols,
                                       gvec, off, elems, pn, amax);
     }
 
@@ -293,14 +332,9 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
     uint32_t under = 0u;
     // chunks j >= jn hold padding only: their new masters are 0, their codes
     // 0x00 (stored only into a folded code shard), their monitor terms 0
-    int jn = kVec;
-    if (PAD) {
-        const int row0 = tid >> 5, col = (tid & 31) << 2;
-        jn = col >= cols ? 0 : min(kVec, max(0, (rows - row0 + 15) >> 4));
-    }
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-        if (PAD && j >= jn) {
+        if (PAD && j >= cp.jn) {
             if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, 0u);
             continue;
         }
@@ -310,12 +344,12 @@ __global__ void __launch_bounds__(kThreads, MON ? 2 : 3) step_kernel(const StepA
         const uint32_t q = lo | (hi << 16);
         if (CODES_FOLDED) __stcs(a.codes + base + j * kThreads, q);
         if (CODES_ROWS) {
-            const int ci = tid + j * kThreads;
+            const int row = cp.rbase + ((16 * j) << (PAD ? cp.sh : 0));
             if (!PAD && cvec) {  // a full tile, 4-byte aligned rows
-                const int64_t at = (int64_t)(ci >> 5) * ld + ((ci & 31) << 2);
+                const int64_t at = (int64_t)row * ld + cp.col;
                 if (in_extent(off + at, 4, elems)) __stcs(reinterpret_cast<unsigned int*>(ctile + at), q);
             } else {
-                store_codes_rows(ctile, ld, ci >> 5, (ci & 31) << 2, rows, cols, cvec, q, off, elems);
+                store_codes_rows(ctile, ld, row, cp.col, rows, cols, cvec, q, off, elems);
             }
         }
         if (MON) {
