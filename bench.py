@@ -557,6 +557,19 @@ def other_workload(spec: str, steps: int, dev, dist, peak: float) -> dict:
     step_bytes = STEP_BYTES_PER_ELEM * n_real + STEP_BYTES_PER_BLOCK * nblk
     norm_bytes = 4 * n_real
     gbs = {"norm": norm_bytes / kern["norm"] / 1e6, "step": step_bytes / kern["step"] / 1e6}
+    # the norm alone, launches back to back: in the loop it follows the step,
+    # whose dirty lines in L2 it writes back as it evicts them
+    sums = torch.zeros(1, dtype=torch.float64, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    alone = []
+    for i in range(steps + 3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        F.fp8z1_fold_norm(opt.layout, gptrs, None, opt.b0, opt.b1, sums, flag, stream)
+        b.record(stream)
+        alone.append((a, b))
+    torch.cuda.synchronize()
+    norm_alone = statistics.median(a.elapsed_time(b) for a, b in alone[3:])
     out = {"workload": _workload_label(argparse.Namespace(workload=name, experts=0, params=0), w.shapes),
            "dp": "whole buffer (1 rank)" if dp == 1 else f"rank {shard_rank} of {dp}: blocks [{opt.b0}, {opt.b1})",
            "blocks": nblk, "elems_padded": n_pad, "elems_real": n_real, "steps": steps, "warmup": 3,
@@ -566,6 +579,10 @@ def other_workload(spec: str, steps: int, dev, dist, peak: float) -> dict:
            "bytes_per_launch": {"fold_norm": norm_bytes, "step": step_bytes},
            "kernels_gbs": {"fold_norm": gbs["norm"], "step": gbs["step"]},
            "frac_of_measured": {"fold_norm": gbs["norm"] / peak, "step": gbs["step"] / peak},
+           "fold_norm_alone": {"ms_median": norm_alone, "gbs": norm_bytes / norm_alone / 1e6,
+                               "frac_of_measured": norm_bytes / norm_alone / 1e6 / peak,
+                               "note": "launches back to back, not after the step: in the loop the norm "
+                                       "also writes back the step's dirty L2 lines as it evicts them"},
            "skipped_steps": skipped, "setup_s": setup_s}
     del opt, grads, fp8, gptrs, fptrs
     torch.cuda.synchronize()
