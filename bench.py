@@ -449,7 +449,7 @@ def bench_ours(args, rank, world, dist):
     # the other configurations, each a few steps of the same loop, after the
     # headline's timed region (its buffers freed first)
     others = None
-    if args.other_workloads and not args.experts and not args.params:
+    if args.other_workloads not in ("", "none") and not args.experts and not args.params:
         del opt, grads, fp8, gptrs, fptrs
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -925,7 +925,7 @@ def main():
                     "instead of the whole buffer (block scheme)")
     ap.add_argument("--other-workloads", default="dense,ragged,moe@8:3,ragged_literal",
                     help="comma-separated configurations (name or name@D:r) timed after the headline "
-                         "for --other-steps steps each in the same loop; empty: none")
+                         "for --other-steps steps each in the same loop; empty or 'none': none")
     ap.add_argument("--other-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=0,

@@ -128,3 +128,4 @@ def test_at_the_block_limit_and_a_range_split_over_two_calls():
     assert abs(split[0].item() - ref[0].item()) <= 1e-12 * total
     del g, host
     torch.cuda.empty_cache()
+
