@@ -77,6 +77,8 @@ def test_bench_line_tiny():
         assert o["steps"] == 3 and o["ms_per_step"] > 0 and o["skipped_steps"] == 0
         assert set(o["kernels_ms"]) == set(o["kernels_gbs"]) == set(o["frac_of_measured"]) == {"fold_norm", "step"}
         assert o["kernels_gbs"]["step"] == pytest.approx(o["bytes_per_launch"]["step"] / o["kernels_ms"]["step"] / 1e6)
+        na = o["fold_norm_alone"]
+        assert na["ms_median"] > 0 and na["gbs"] == pytest.approx(o["bytes_per_launch"]["fold_norm"] / na["ms_median"] / 1e6)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
     assert len(e["ms_per_step_reps"]) == len(e["ms_per_step_one_at_a_time_reps"]) == e["reps"] == 3

@@ -25,10 +25,12 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 # every GPU test file that drives the library through Python (the maximum-size
 # one included: a weight past 2^31 elements, where offsets need 64 bits),
-# minus the ones that run the bench or link the library from C
+# minus the ones that run the bench or link the library from C, and the
+# literal ragged workload (160 GB on the device; the small-block file covers
+# its block shapes)
 SUITES = ["test_gpu_fold.py", "test_gpu_norm.py", "test_gpu_step.py", "test_gpu_fused.py", "test_gpu_next.py",
           "test_gpu_graph.py", "test_gpu_resume.py", "test_gpu_workloads.py", "test_gpu_maxsize.py",
-          "test_gpu_random_layouts.py", "test_zz_no_alloc.py"]
+          "test_gpu_random_layouts.py", "test_gpu_small_blocks.py", "test_zz_no_alloc.py"]
 
 
 def test_parity_suites_on_the_checked_build(lib):
