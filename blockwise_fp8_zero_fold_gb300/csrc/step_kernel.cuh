@@ -153,9 +153,6 @@ __device__ __forceinline__ void monitor_add(float p, float dec, float scale, flo
 // slower on MoE (7.37 against 6.78 ms).
 constexpr int kMasterSmemBytes = kThreads * kVec * 16;
 
-// The update of this thread's 8 float4 chunks of the block: new masters into
-// pn[j * kThreads] (shared memory), their largest magnitude into amax.  PAD: skip the chunks that hold
-// padding only (chunk j of thread t is row t/32 + 16 j, columns 4 (t%32) .. +3).
 // Where this thread's chunks of a block sit.  A warp takes 32 / W rows at a
 // time, W = the block's real chunks a row rounded up to a power of two (sh =
 // log2(32 / W); sh = 0 for a block with more than 64 real columns and in
@@ -186,6 +183,9 @@ __device__ __forceinline__ ChunkPlace chunk_place(int64_t kb, int tid, int rows,
     return c;
 }
 
+// The update of this thread's 8 float4 chunks of the block (placed by cp):
+// new masters into pn[j * kThreads] (shared memory), their largest magnitude
+// into amax.  PAD: the chunks j >= cp.jn hold padding only and are skipped.
 template <bool GRAD_ROWS, bool PAD>
 __device__ __forceinline__ void update_chunks(const StepArgs& a, const StepScalars& c, float gs, const ChunkPlace& cp,
                                               const float* gtile, int64_t ld, int rows, int cols,
