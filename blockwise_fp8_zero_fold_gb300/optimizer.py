@@ -61,9 +61,10 @@ class _AsyncSteps:
     hyper-parameter sets (step k-1 clean: t+1 and S after growth; skipped: t
     and S/2), and its kernel picks one by step k-1's found_inf (the *_select
     entry points).  Each step's norm accumulators alternate between two slots,
-    and its found_inf is copied to pinned memory right after its norm; the
-    host waits only for that copy of step k-2 before enqueuing step k.
-    Results equal the synchronous steps'."""
+    and its found_inf is copied to pinned memory right after its norm, on a
+    side stream, so that the update does not wait for the copy; the host waits
+    only for that copy of step k-2 before enqueuing step k (whose norm then
+    reuses the slot).  Results equal the synchronous steps'."""
 
     def _async_launch(self, norm, step, stream, events) -> List[int]:
         """norm(sumsq, found, s) enqueues the norm; step(hp, hp_if_set,
@@ -76,6 +77,8 @@ class _AsyncSteps:
                 "found": torch.zeros(2, dtype=torch.int32, device=self.device),
                 "flags": [torch.zeros(1, dtype=torch.int32, pin_memory=True) for _ in range(2)],
                 "done": [torch.cuda.Event() for _ in range(2)],
+                "normed": [torch.cuda.Event() for _ in range(2)],
+                "side": torch.cuda.Stream(self.device),  # the flag copies
                 "k": 0, "inflight": [],  # slots of unresolved steps, oldest first
             }
         s = self._torch_stream(stream, self.device)
@@ -95,9 +98,12 @@ class _AsyncSteps:
                 self.norm_hook(sumsq, found)
         if "norm" in ev:
             ev["norm"][1].record(s)
-        with torch.cuda.stream(s):
+        st["normed"][slot].record(s)
+        side = st["side"]
+        side.wait_event(st["normed"][slot])
+        with torch.cuda.stream(side):
             st["flags"][slot].copy_(found, non_blocking=True)
-        st["done"][slot].record(s)
+        st["done"][slot].record(side)
         if "step" in ev:
             ev["step"][0].record(s)
         if not st["inflight"]:
