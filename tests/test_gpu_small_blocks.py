@@ -1,10 +1,12 @@
 """GPU parity of the fused step on layouts made of small and partial blocks
 ("面向 Blockwise FP8 量化的 ZeRO 优化器设计" §块粒度切分: padding to multiples
 of 128 leaves partial blocks on every weight whose R or C is not one): forty
-one-block weights, one-row and one-column weights, C < 4 and every C % 4,
-weights whose storage starts 1-3 elements into a buffer, full tiles among the
-partial ones, a 512-block full-tile run between padded weights, the three
-scalar forms, a skipped step and an unreadable param.
+one-block weights, one-row and one-column weights, C < 4 and every C % 4, real
+columns and rows on either side of each point where a warp starts taking
+several rows of a narrow block, weights whose storage starts 1-3 elements into
+a buffer, full tiles among the partial ones, a 512-block full-tile run between
+padded weights, the three scalar forms, a skipped step and an unreadable
+param.
 
 Every case is compared with the oracle -- master / m / v / scales bit for
 bit, the row-major codes byte for byte, every code outside the real elements
@@ -28,6 +30,11 @@ CASES = {
     "narrow_and_flat": [(1, 300, 1), (1, 1, 300), (2, 129, 3), (1, 5, 2), (3, 1, 1), (1, 700, 6)],
     "ragged_mix": [(1, 17, 690), (2, 255, 3), (3, 129, 257), (1, 1000, 131), (1, 128, 384), (2, 200, 130)],
     "every_c_mod_4": [(1, 150 + k, 260 + k) for k in range(8)],
+    # real columns on either side of every warp-row split (a warp takes 32 / W rows
+    # of a block whose real chunks a row fit in W = 16, 8, 4, 2, 1), rows on either
+    # side of a task and of a warp's share
+    "row_split_edges": [(1, r, c) for c in (4, 5, 8, 9, 16, 17, 32, 33, 64, 65, 127, 129)
+                        for r in (1, 31, 33, 97, 130)],
 }
 
 
