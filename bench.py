@@ -915,7 +915,7 @@ def main():
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
     ap.add_argument("--e2e-steps", type=int, default=8)
-    ap.add_argument("--e2e-reps", type=int, default=3,
+    ap.add_argument("--e2e-reps", type=int, default=5,
                     help="repetitions of each e2e form (alternating); the medians are reported")
     ap.add_argument("--monitors", type=int, default=0,
                     help="also time N launches of the fused step with the per-block quantisation monitors")
