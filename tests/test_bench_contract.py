@@ -81,7 +81,7 @@ def test_bench_line_tiny():
         assert na["ms_median"] > 0 and na["gbs"] == pytest.approx(o["bytes_per_launch"]["fold_norm"] / na["ms_median"] / 1e6)
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] == 4 * 60000 and e["d2h_bytes_per_step"] > 60000
-    assert len(e["ms_per_step_reps"]) == len(e["ms_per_step_one_at_a_time_reps"]) == e["reps"] == 3
+    assert len(e["ms_per_step_reps"]) == len(e["ms_per_step_one_at_a_time_reps"]) == e["reps"] == 5
     assert e["ms_per_step"] == sorted(e["ms_per_step_reps"])[1]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] > 0
     assert d["other_path"]["path"] == "unfused"
