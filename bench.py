@@ -453,8 +453,9 @@ def bench_ours(args, rank, world, dist):
         del opt, grads, fp8, gptrs, fptrs
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        others = [other_workload(spec, args.other_steps, dev, dist, peak) for spec in
-                  args.other_workloads.split(",") if spec]
+        others = [other_workload_mx(spec[3:], args.other_steps, dev, dist, peak) if spec.startswith("mx:")
+                  else other_workload(spec, args.other_steps, dev, dist, peak)
+                  for spec in args.other_workloads.split(",") if spec]
 
     out = {
         "metric": METRIC,
@@ -590,6 +591,75 @@ def other_workload(spec: str, steps: int, dev, dist, peak: float) -> dict:
     return out
 
 
+def other_workload_mx(name: str, steps: int, dev, dist, peak: float) -> dict:
+    """The MXFP8 variant on workload ``name`` (whole buffer) in its pipelined
+    loop, ``steps`` timed steps after 3 warm-up steps; the same record as
+    ``other_workload`` (bytes: 4 per element for the norm, 29 per element plus
+    the E8M0 scales for the step)."""
+    import torch
+
+    from blockwise_fp8_zero_fold_gb300 import fp8z1 as F
+    from blockwise_fp8_zero_fold_gb300 import synth
+    from blockwise_fp8_zero_fold_gb300.optimizer import MxShardOptimizer
+
+    w = synth.workload(name, dp=1, rank=0)
+    t_setup = time.perf_counter()
+    opt = MxShardOptimizer(w.shapes, device=dev, loss_scale=w.loss_scale, growth_interval=w.growth_interval,
+                           **{k: v for k, v in w.hp().items() if k != "loss_scale"})
+    n = opt.n_elems
+    for kind, buf in (("master", opt.master), ("m", opt.m), ("v", opt.v)):
+        _flat_into(buf, synth.make_state(w, kind, dev))
+    grad = torch.empty(n, dtype=torch.float32, device=dev)
+    _flat_into(grad, synth.make_grads(w, 1, dev))
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        opt.launch_step_async(grad, stream)
+    opt.drain()
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)] for k in ("norm", "step")}
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    skipped = 0
+    for i in range(steps):
+        skipped += sum(opt.launch_step_async(grad, stream, {"norm": ev["norm"][i], "step": ev["step"][i]}))
+    skipped += sum(opt.drain())
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev) / steps
+    kern = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    med = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    step_bytes, norm_bytes = 29 * n + n // 32, 4 * n
+    gbs = {"norm": norm_bytes / kern["norm"] / 1e6, "step": step_bytes / kern["step"] / 1e6}
+    out = {"workload": _workload_label(argparse.Namespace(workload=name, experts=0, params=0), w.shapes)
+                       + " in the MXFP8 layout (E8M0 scale per 32 elements)",
+           "scheme": "mx", "dp": "whole buffer (1 rank)", "groups": opt.n_groups, "elems_padded": n,
+           "elems_real": n, "steps": steps, "warmup": 3, "ms_per_step": ms, "value": n / (ms / 1e3),
+           "real_elem_per_s": n / (ms / 1e3),
+           "kernels_ms": {"norm": kern["norm"], "step": kern["step"]},
+           "kernels_ms_median": {"norm": med["norm"], "step": med["step"]},
+           "bytes_per_launch": {"norm": norm_bytes, "step": step_bytes},
+           "kernels_gbs": gbs, "frac_of_measured": {k: v / peak for k, v in gbs.items()},
+           "whole_step_gbs": (norm_bytes + step_bytes) / ms / 1e6,
+           "skipped_steps": skipped, "setup_s": setup_s}
+    del opt, grad
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def _flat_into(dst, tensors):
+    """The tensors' elements back to back into the flat buffer ``dst``."""
+    off = 0
+    for t in tensors:
+        dst[off:off + t.numel()].copy_(t.reshape(-1))
+        off += t.numel()
+
+
 def bench_mx(args, rank, world, dist):
     """The MXFP8 variant on the same workload: flat row-major state, a step is
     the grad norm + the fused update with the MX quantiser (no fold, no table)."""
@@ -613,17 +683,10 @@ def bench_mx(args, rank, world, dist):
                            growth_interval=w.growth_interval,
                            **{k: v for k, v in w.hp().items() if k != "loss_scale"})
     n = opt.n_elems
-
-    def flat_into(dst, tensors):
-        off = 0
-        for t in tensors:
-            dst[off:off + t.numel()].copy_(t.reshape(-1))
-            off += t.numel()
-
     for kind, buf in (("master", opt.master), ("m", opt.m), ("v", opt.v)):
-        flat_into(buf, synth.make_state(w, kind, dev))
+        _flat_into(buf, synth.make_state(w, kind, dev))
     grad = torch.empty(n, dtype=torch.float32, device=dev)
-    flat_into(grad, synth.make_grads(w, 1, dev))
+    _flat_into(grad, synth.make_grads(w, 1, dev))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -923,9 +986,10 @@ def main():
                     help="also time N launches each of the bf16 fold and unfold of the weights")
     ap.add_argument("--shard", default="", help="D:r -- time DP rank r's block range of D ranks "
                     "instead of the whole buffer (block scheme)")
-    ap.add_argument("--other-workloads", default="dense,ragged,moe@8:3,ragged_literal",
-                    help="comma-separated configurations (name or name@D:r) timed after the headline "
-                         "for --other-steps steps each in the same loop; empty or 'none': none")
+    ap.add_argument("--other-workloads", default="dense,ragged,moe@8:3,ragged_literal,large,mx:moe",
+                    help="comma-separated configurations (name, name@D:r, or mx:name for the MXFP8 "
+                         "variant) timed after the headline for --other-steps steps each in the same "
+                         "loop; empty or 'none': none")
     ap.add_argument("--other-steps", type=int, default=20)
     ap.add_argument("--cpu-sample-experts", type=int, default=6)
     ap.add_argument("--ref-sample-experts", type=int, default=0,

@@ -69,11 +69,18 @@ def _check_ours(d, steps):
 @pytest.mark.gpu
 def test_bench_line_tiny():
     d = _run("--workload", "tiny", "--steps", "4", "--warmup", "3", "--compare", "1", "--e2e-steps", "2",
-             "--cpu-sample-experts", "1", "--monitors", "2", "--other-workloads", "tiny,tiny@2:1",
+             "--cpu-sample-experts", "1", "--monitors", "2", "--other-workloads", "tiny,tiny@2:1,mx:moe",
              "--other-steps", "3")
     _check_ours(d, 4)
-    ow = d["other_workloads"]
+    ow, mx = d["other_workloads"][:2], d["other_workloads"][2]
     assert [o["blocks"] for o in ow] == [6, 3] and ow[1]["dp"].startswith("rank 1 of 2")
+    # the MXFP8 variant's record: the norm and the step, 4 and 29 B per element (+ scales)
+    n = 32 * (7168 * 4096 + 2048 * 7168)
+    assert mx["scheme"] == "mx" and mx["elems_padded"] == mx["elems_real"] == n and mx["groups"] == n // 32
+    assert mx["steps"] == 3 and mx["ms_per_step"] > 0 and mx["skipped_steps"] == 0
+    assert mx["bytes_per_launch"] == {"norm": 4 * n, "step": 29 * n + n // 32}
+    for k in ("norm", "step"):
+        assert mx["kernels_gbs"][k] == pytest.approx(mx["bytes_per_launch"][k] / mx["kernels_ms"][k] / 1e6)
     for o in ow:
         assert o["steps"] == 3 and o["ms_per_step"] > 0 and o["skipped_steps"] == 0
         assert set(o["kernels_ms"]) == set(o["kernels_gbs"]) == set(o["frac_of_measured"]) == {"fold_norm", "step"}
