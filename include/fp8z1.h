@@ -304,7 +304,8 @@ int fp8z1_fold_norm(const fp8z1_layout* layout, const float* const* d_grad_param
  * and of grad_shard when given, zero and neither read nor written).  A null
  * grad or FP8 param pointer (or a grad pointer that is not
  * 4-byte aligned) leaves that block untouched and sets
- * FP8Z1_DEVSTATUS_BADPTR.
+ * FP8Z1_DEVSTATUS_BADPTR.  The row-major grads may be read through the
+ * read-only data path: nothing may write them while the step runs.
  * Quantisation monitors ("FP8训练技术与万亿参数模型优化实践" §1.2: underflow =
  * zeros / total, healthy below 0.5%; distortion = cosine(original,
  * dequantised), healthy above 0.995): when `block_cos` and
