@@ -403,11 +403,25 @@ def bench_ours(args, rank, world, dist):
     # and the FP8 weights + scales + found flag read back every step
     e2e = None
     if args.e2e_steps > 0 and whole:
-        hgrads = [torch.empty(s, dtype=torch.float32, pin_memory=True) for s in w.shapes]
+        # every rank pins its own host buffers (7 GB for MoE): all ranks go on,
+        # or all report e2e unavailable, so none waits at a barrier alone
+        why = ""
+        try:
+            hgrads = [torch.empty(s, dtype=torch.float32, pin_memory=True) for s in w.shapes]
+            hfp8 = [torch.empty(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
+            hscales = torch.empty(nblk, dtype=torch.float32, pin_memory=True)
+        except RuntimeError as exc:
+            why = str(exc).strip().splitlines()[0][:200] if str(exc).strip() else type(exc).__name__
+            hgrads = hfp8 = hscales = None
+        ok = torch.tensor([0 if why else 1], dtype=torch.int32, device=dev)
+        if dist is not None:
+            dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if not int(ok.item()):
+            e2e = {"value": None, "unit": "elem/s",
+                   "unavailable": "pinned host buffers could not be allocated" + (f": {why}" if why else " on another rank")}
+    if e2e is None and args.e2e_steps > 0 and whole:
         for h, d in zip(hgrads, grads):
             h.copy_(d)
-        hfp8 = [torch.empty(s, dtype=torch.uint8, pin_memory=True) for s in w.shapes]
-        hscales = torch.empty(nblk, dtype=torch.float32, pin_memory=True)
         h2d = sum(h.numel() * 4 for h in hgrads)
         d2h = sum(h.numel() for h in hfp8) + nblk * 4 + 4
 
