@@ -991,7 +991,7 @@ def main():
                          "(launch_step_async); -1: on for MX and the block scheme's fused path")
     ap.add_argument("--params", type=int, default=0,
                     help="keep only the first K params of the workload (a smaller case)")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--e2e-reps", type=int, default=5,
                     help="repetitions of each e2e form (alternating); the medians are reported")
     ap.add_argument("--monitors", type=int, default=0,
