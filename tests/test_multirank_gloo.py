@@ -1,4 +1,4 @@
-"""Multi-rank host logic on CPU with world_size-2 gloo process groups.
+"""Multi-rank host logic on CPU with gloo process groups of 2 and 4 ranks.
 
 1. The data-parallel flow of "面向 Blockwise FP8 量化的 ZeRO 优化器设计" §总结
    with real ranks: each rank takes its block range from the C-ABI's host
@@ -73,22 +73,27 @@ def _dp_worker(rank, world, port, shapes, result_q):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("shapes", [[(1, 300, 200)], [(3, 129, 257), (1, 17, 690)]])
-def test_two_rank_step_equals_one_rank(shapes):
+@pytest.mark.parametrize("shapes,world", [([(1, 300, 200)], 2), ([(3, 129, 257), (1, 17, 690)], 2),
+                                          ([(1, 300, 200)], 4)])
+def test_multi_rank_step_equals_one_rank(shapes, world):
+    """world ranks step their block ranges and exchange; with 6 blocks over 4
+    ranks the last rank's range is empty and it still joins both exchanges."""
     import oracle
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_dp_worker, args=(r, 2, port, shapes, q)) for r in range(2)]
+    procs = [ctx.Process(target=_dp_worker, args=(r, world, port, shapes, q)) for r in range(world)]
     for p in procs:
         p.start()
-    outs = [q.get(timeout=120) for _ in range(2)]
+    outs = [q.get(timeout=120) for _ in range(world)]
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
     ranges = sorted((o[0], o[1]) for o in outs)
     nblk = oracle.count_blocks(shapes)
-    assert ranges[0][0] == 0 and ranges[0][1] == ranges[1][0] and ranges[1][1] == nblk
+    assert ranges == [oracle.shard_range(nblk, world, r) for r in range(world)]
+    assert ranges[0][0] == 0 and ranges[-1][1] == nblk
+    assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
     codes, scales = next((o[2], o[3]) for o in outs if o[2] is not None)
     # the same step on one rank owning everything
     rng = np.random.default_rng(0)
@@ -97,8 +102,9 @@ def test_two_rank_step_equals_one_rank(shapes):
     g = oracle.fold(shapes, rows)
     p = oracle.fold(shapes, master)
     s_total, _ = oracle.sumsq(g)
-    # two partials added in double: within one rounding of the exact sum
-    assert abs(outs[0][4] - s_total) <= 2 ** -52 * s_total
+    # the partials added in double: within a few roundings of the exact sum
+    assert all(o[4] == outs[0][4] for o in outs)
+    assert abs(outs[0][4] - s_total) <= world * 2 ** -52 * s_total
     hp = oracle.make_hp(1e-3, 0.9, 0.95, 1e-8, 0.1, 0.5, 1024.0, 1)
     q1, s1, _ = oracle.step(hp, outs[0][4], 0, g, p, np.zeros_like(p), np.zeros_like(p))
     assert np.array_equal(codes, q1) and np.array_equal(scales, s1)
